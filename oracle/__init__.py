@@ -1,0 +1,271 @@
+"""Plain f64 CPU oracle for fused paged-attention decode v2.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s cpu_baseline / ``--impl reference`` legs import this package.
+The product path (``paged_attention_decode_gb300``) never imports it, and the
+two share no code: the arithmetic lives in ``pa_oracle.c`` (plain C, double
+precision, see its header for the passage each function follows) and this
+module only marshals arrays into it.
+
+Cascade composition (``cascade_ref``) follows cascade-attention.md (issue
+#903): level 0 attends the shared span once with the members' query heads
+stacked ``h0 = kv * (M * G) + m * G + g``, level 1 attends each member's
+private suffix, and one merge pairs each member's two states.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_pa.so")
+
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+# geometry validation codes, mirroring the enum in pa_oracle.c
+GEOM_OK = 0
+GEOM_BAD_ARGS = 1
+GEOM_INDPTR0 = 2
+GEOM_INDPTR_ORDER = 3
+GEOM_LAST_PAGE_LEN = 4
+GEOM_FIRST_OFFSET = 5
+GEOM_SINGLE_PAGE = 6
+GEOM_EMPTY_REQUEST = 7
+GEOM_PAGE_ID = 8
+GEOM_IDENTITY = 9
+
+MAX_CHUNKS = 65535
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c into liboracle_pa.so next to it (gcc, OpenMP if available)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+            "-D_GNU_SOURCE", _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        L.ora_decode_element.argtypes = [P, i32, i64]
+        L.ora_decode_element.restype = f64
+        L.ora_num_threads.restype = i32
+        L.ora_seq_len.argtypes = [P, P, P, i32, i32]
+        L.ora_seq_len.restype = i64
+        L.ora_validate_geometry.argtypes = [P, P, P, i32, i32, P, i64, P]
+        L.ora_validate_geometry.restype = i32
+        L.ora_resolve_row.argtypes = [P, P, P, i32, i32, i64]
+        L.ora_resolve_row.restype = i64
+        L.ora_attention.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32, f64, P, P]
+        L.ora_attention.restype = None
+        L.ora_partials.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32, P, P, i64, f64, P, P]
+        L.ora_partials.restype = None
+        L.ora_merge.argtypes = [P, P, P, i32, i32, i32, P, P]
+        L.ora_merge.restype = None
+        L.ora_plan.argtypes = [P, i32, i32, i32, i64, i32, i64, P, P, P, P, P, P, i64, P]
+        L.ora_plan.restype = i32
+        _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().ora_num_threads())
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _i32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=np.int32)
+
+
+def _f32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().float().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=np.float32)
+
+
+def _f64(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=np.float64)
+
+
+def _pool(t: torch.Tensor):
+    """A CPU contiguous pool tensor and its dtype code (raw storage is read by C)."""
+    t = t.detach().cpu().contiguous()
+    return t, DTYPE_CODES[t.dtype]
+
+
+def _ptr(a) -> int:
+    if isinstance(a, torch.Tensor):
+        return a.data_ptr()
+    return a.ctypes.data
+
+
+# ---------------------------------------------------------------------------
+# public oracle API
+# ---------------------------------------------------------------------------
+
+def decode_elements(t: torch.Tensor) -> np.ndarray:
+    """Every element of a CPU tensor decoded to f64 by the oracle's own decoder."""
+    t, code = _pool(t)
+    flat = t.reshape(-1)
+    L = lib()
+    return np.array([L.ora_decode_element(_ptr(flat), code, i) for i in range(flat.numel())])
+
+
+def seq_lens(indptr, last_page_len, first_page_offset, page_size) -> list[int]:
+    ip, lp, fp = _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    return [int(lib().ora_seq_len(_ptr(ip), _ptr(lp), _ptr(fp), page_size, r)) for r in range(len(lp))]
+
+
+def validate_geometry(indptr, last_page_len, first_page_offset, page_size, indices=None,
+                      num_pages=0, expect_seq_lens: Sequence[int] | None = None) -> int:
+    ip, lp, fp = _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    batch = len(lp)
+    idx = _i32(indices) if indices is not None else None
+    sl = np.ascontiguousarray(np.asarray(expect_seq_lens, dtype=np.int64)) if expect_seq_lens is not None else None
+    return int(lib().ora_validate_geometry(_ptr(ip), _ptr(lp), _ptr(fp), batch, page_size,
+                                           _ptr(idx) if idx is not None else None, int(num_pages),
+                                           _ptr(sl) if sl is not None else None))
+
+
+def resolve_rows(indices, indptr, first_page_offset, page_size, r: int, n: int) -> list[int]:
+    """Pool rows (page * page_size + entry) of visible tokens 0..n-1 of request r."""
+    idx, ip, fp = _i32(indices), _i32(indptr), _i32(first_page_offset)
+    L = lib()
+    return [int(L.ora_resolve_row(_ptr(idx), _ptr(ip), _ptr(fp), page_size, r, i)) for i in range(n)]
+
+
+def attention(q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, scale):
+    """Decode attention for every (request, query head): (out [B,Hq,D] f64, lse2 [B,Hq] f64)."""
+    qf = _f32(q)
+    B, Hq, D = qf.shape
+    kp, code = _pool(k_pool)
+    vp, code_v = _pool(v_pool)
+    assert code == code_v and kp.shape == vp.shape
+    P, ps, Hkv, Dk = kp.shape
+    assert Dk == D
+    idx, ip, lp, fp = _i32(indices), _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    lib().ora_attention(_ptr(qf), _ptr(kp), _ptr(vp), code, _ptr(idx), _ptr(ip), _ptr(lp), _ptr(fp),
+                        B, Hq, Hkv, D, ps, float(scale), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def partials(q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, scale,
+             pages_per_chunk, request_indices, kv_tile_indices):
+    """Per-chunk normalized partials and base-2 LSEs: (v [N,Hq,D] f64, lse2 [N,Hq] f64)."""
+    qf = _f32(q)
+    B, Hq, D = qf.shape
+    kp, code = _pool(k_pool)
+    vp, _ = _pool(v_pool)
+    P, ps, Hkv, _ = kp.shape
+    idx, ip, lp, fp = _i32(indices), _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    ri, ti = _i32(request_indices), _i32(kv_tile_indices)
+    N = len(ri)
+    out = np.zeros((N, Hq, D), np.float64)
+    lse = np.zeros((N, Hq), np.float64)
+    lib().ora_partials(_ptr(qf), _ptr(kp), _ptr(vp), code, _ptr(idx), _ptr(ip), _ptr(lp), _ptr(fp),
+                       Hq, Hkv, D, ps, int(pages_per_chunk), _ptr(ri), _ptr(ti), N, float(scale),
+                       _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def merge(v_in, lse_in, o_indptr):
+    """Closed-form merge of attention states grouped by o_indptr: (out [M,H,D], lse2 [M,H])."""
+    v, l, oi = _f64(v_in), _f64(lse_in), _i32(o_indptr)
+    N, H, D = v.shape
+    M = len(oi) - 1
+    out = np.zeros((M, H, D), np.float64)
+    lse = np.zeros((M, H), np.float64)
+    lib().ora_merge(_ptr(v), _ptr(l), _ptr(oi), M, H, D, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+class PlanRef:
+    """Result of the oracle plan (linear scan over every chunk size)."""
+
+    def __init__(self, pages_per_chunk, lo, hi, num_chunks, request_indices, kv_tile_indices, o_indptr):
+        self.pages_per_chunk = pages_per_chunk
+        self.lo = lo
+        self.hi = hi
+        self.num_chunks = num_chunks
+        self.request_indices = request_indices
+        self.kv_tile_indices = kv_tile_indices
+        self.o_indptr = o_indptr
+
+    @property
+    def needs_merge(self) -> bool:
+        return self.num_chunks > len(self.o_indptr) - 1
+
+
+def plan(indptr, num_kv_heads: int, q_groups: int, target_ctas: int, ppc_override: int = 0,
+         max_chunks: int = MAX_CHUNKS) -> PlanRef:
+    ip = _i32(indptr)
+    batch = len(ip) - 1
+    cap = int(sum(max(1, int(ip[r + 1] - ip[r])) for r in range(batch)))
+    ri = np.zeros(max(cap, 1), np.int32)
+    ti = np.zeros(max(cap, 1), np.int32)
+    oi = np.zeros(batch + 1, np.int32)
+    ppc, lo, hi = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    n = ctypes.c_int64()
+    rc = lib().ora_plan(_ptr(ip), batch, num_kv_heads, q_groups, int(target_ctas), int(ppc_override),
+                        int(max_chunks), ctypes.addressof(ppc), ctypes.addressof(lo), ctypes.addressof(hi),
+                        ctypes.addressof(n), _ptr(ri), _ptr(ti), cap, _ptr(oi))
+    if rc != 0:
+        raise ValueError(f"oracle plan failed with code {rc}")
+    N = int(n.value)
+    return PlanRef(int(ppc.value), int(lo.value), int(hi.value), N, ri[:N].copy(), ti[:N].copy(), oi)
+
+
+def cascade_ref(q, k_pool, v_pool, prefix_indices, suffix_indices, suffix_indptr,
+                suffix_last_page_len, scale):
+    """Two-level cascade decode of M members sharing a whole-page prefix.
+
+    q: [M, Hq, D].  The prefix pages (all full) are attended once as one
+    request whose query heads are the members' heads stacked
+    h0 = kv * (M * G) + m * G + g; each member's suffix pages are attended as
+    its own request; the two states of member m are merged.  Returns
+    (out [M, Hq, D] f64, lse2 [M, Hq] f64).
+    """
+    qf = torch.as_tensor(_f32(q))
+    M, Hq, D = qf.shape
+    P, ps, Hkv, _ = k_pool.shape
+    G = Hq // Hkv
+    # level 0: [M, Hkv, G, D] -> [Hkv, M, G, D], one request with M*Hq heads
+    q0 = qf.reshape(M, Hkv, G, D).permute(1, 0, 2, 3).reshape(1, Hkv * M * G, D)
+    npre = len(prefix_indices)
+    o0, l0 = attention(q0, k_pool, v_pool, prefix_indices, [0, npre], [ps if npre else 0], [0], scale)
+    o0 = torch.from_numpy(o0).reshape(Hkv, M, G, D).permute(1, 0, 2, 3).reshape(M, Hq, D)
+    l0 = torch.from_numpy(l0).reshape(Hkv, M, G).permute(1, 0, 2).reshape(M, Hq)
+    # level 1: each member's private suffix
+    o1, l1 = attention(qf, k_pool, v_pool, suffix_indices, suffix_indptr, suffix_last_page_len,
+                       [0] * M, scale)
+    v_in = torch.stack([o0, torch.from_numpy(o1)], dim=1).reshape(2 * M, Hq, D)
+    lse_in = torch.stack([l0, torch.from_numpy(l1)], dim=1).reshape(2 * M, Hq)
+    return merge(v_in, lse_in, list(range(0, 2 * M + 1, 2)))

@@ -1,0 +1,301 @@
+"""Seeded synthetic inputs for paged-attention decode.
+
+This module only builds inputs: a CSR page table over a paged KV pool, the
+pools themselves and the query.  It holds none of the attention arithmetic
+and imports neither the CUDA binding nor the oracle, so the GPU path and the
+oracle can both be fed from it.
+
+Layouts (issue #898, Task 1 and design piece 1; PR #984, What changed 1):
+
+- ``k_pool``/``v_pool``: ``[num_pages, page_size, num_kv_heads, head_dim]``,
+  one contiguous buffer per side.
+- ``indices`` (int32, flat physical page ids), ``indptr`` (int32, ``[B+1]``),
+  ``last_page_len`` (int32, ``[B]``, valid entries of the final page, equal to
+  ``page_size`` when that page is exactly full) and ``first_page_offset``
+  (int32, ``[B]``, the entry of the first page where a sliding window starts).
+- ``q``: ``[B, Hq, head_dim]`` float32.
+
+All random values are N(0, 1) from a CPU ``torch.Generator`` seeded per
+workload, cast to the pool dtype; consumers read the cast values.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Sequence
+
+import torch
+
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
+
+
+@dataclass
+class PagedBatch:
+    """One decode step's inputs (all tensors on the CPU)."""
+
+    name: str
+    q: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    indices: torch.Tensor
+    indptr: torch.Tensor
+    last_page_len: torch.Tensor
+    first_page_offset: torch.Tensor
+    seq_lens: list[int]
+    page_size: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    scale: float
+    ppc_override: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.seq_lens)
+
+    @property
+    def num_pages(self) -> int:
+        return self.k_pool.shape[0]
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.k_pool.dtype
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V the step must read: every visible token, every KV head, both sides."""
+        return sum(self.seq_lens) * self.num_kv_heads * self.head_dim * 2 * self.k_pool.element_size()
+
+    def to(self, device) -> "PagedBatch":
+        moved = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.__dict__.items()}
+        return PagedBatch(**moved)
+
+
+def page_geometry(seq_len: int, first_page_offset: int, page_size: int) -> tuple[int, int]:
+    """(pages, last_page_len) of a request whose window starts at entry ``first_page_offset``.
+
+    A request with no visible token owns no page and has last_page_len 0.
+    """
+    if seq_len == 0:
+        return 0, 0
+    end = first_page_offset + seq_len          # entries used, counted from the first page's entry 0
+    pages = -(-end // page_size)
+    return pages, end - (pages - 1) * page_size
+
+
+def _randn(gen: torch.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
+    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(dtype)
+
+
+def make_batch(name: str, seq_lens: Sequence[int], first_page_offsets: Sequence[int], page_size: int,
+               num_qo_heads: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype, seed: int,
+               slack: float = 2.0, num_pages: int | None = None, order: str = "shuffled",
+               scale: float | None = None, ppc_override: int = 0) -> PagedBatch:
+    """A batch whose requests own disjoint physical pages drawn from a pool with slack.
+
+    ``order``: "shuffled" (a random permutation of pool pages), "reversed"
+    (pages handed out from the top of the pool downwards) or "identity"
+    (contiguous ascending pages).
+    """
+    gen = torch.Generator().manual_seed(seed)
+    B = len(seq_lens)
+    geo = [page_geometry(s, f, page_size) for s, f in zip(seq_lens, first_page_offsets)]
+    total = sum(p for p, _ in geo)
+    P = num_pages if num_pages is not None else max(1, int(math.ceil(total * slack)))
+    assert P >= total, "pool too small for the batch"
+    if order == "shuffled":
+        ids = torch.randperm(P, generator=gen)[:total]
+    elif order == "reversed":
+        ids = torch.arange(P - 1, P - 1 - total, -1)
+    elif order == "identity":
+        ids = torch.arange(total)
+    else:
+        raise ValueError(order)
+    indptr = [0]
+    for p, _ in geo:
+        indptr.append(indptr[-1] + p)
+    q = torch.randn(B, num_qo_heads, head_dim, generator=gen, dtype=torch.float32)
+    k_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    v_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    return PagedBatch(
+        name=name, q=q, k_pool=k_pool, v_pool=v_pool,
+        indices=ids.to(torch.int32),
+        indptr=torch.tensor(indptr, dtype=torch.int32),
+        last_page_len=torch.tensor([l for _, l in geo], dtype=torch.int32),
+        first_page_offset=torch.tensor([f if s > 0 else 0 for s, f in zip(seq_lens, first_page_offsets)],
+                                       dtype=torch.int32),
+        seq_lens=list(seq_lens), page_size=page_size, num_qo_heads=num_qo_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim,
+        scale=scale if scale is not None else 1.0 / math.sqrt(head_dim),
+        ppc_override=ppc_override)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+def tiny_csr(seed: int = 1000) -> PagedBatch:
+    """B=2, Hq=4, Hkv=2, D=64, page_size=4, seq_lens {13, 7}, first_page_offset {0, 2},
+    a 16-page fp32 pool with shuffled page ids, chunks fixed at 2 pages then merged."""
+    return make_batch("tiny_csr", [13, 7], [0, 2], page_size=4, num_qo_heads=4, num_kv_heads=2,
+                      head_dim=64, dtype=torch.float32, seed=seed, num_pages=16, ppc_override=2)
+
+
+def llama3_8b_32k(seed: int = 1001, context: int = 32768) -> PagedBatch:
+    """Llama-3-8B-shaped single-sequence decode: B=1, Hq=32, Hkv=8, D=128, fp16 pools,
+    page_size=16, 32768 tokens on a random permutation of a pool with 2x slack."""
+    return make_batch("llama3_8b_32k", [context], [0], page_size=16, num_qo_heads=32, num_kv_heads=8,
+                      head_dim=128, dtype=torch.float16, seed=seed, slack=2.0)
+
+
+def sliding_window_batch(seed: int = 1002) -> PagedBatch:
+    """B=4, Hq=32, Hkv=8, D=128, bf16, page_size=16.  Requests 0-1 are 4096-token windows
+    starting mid-page (first_page_offset uniform in [1, 15], retired pages not in the table);
+    requests 2-3 have seq_len uniform in [1024, 16384] starting at entry 0."""
+    gen = torch.Generator().manual_seed(seed)
+    fpo = [int(torch.randint(1, 16, (1,), generator=gen)) for _ in range(2)] + [0, 0]
+    lens = [4096, 4096] + [int(torch.randint(1024, 16385, (1,), generator=gen)) for _ in range(2)]
+    return make_batch("sliding_window_batch", lens, fpo, page_size=16, num_qo_heads=32, num_kv_heads=8,
+                      head_dim=128, dtype=torch.bfloat16, seed=seed + 7, slack=2.0)
+
+
+def sparse_token_exact(seed: int = 1003, batch: int = 2, heads: int = 8, cap: int = 131072,
+                       head_dim: int = 128, n_rep: int = 4, selected: int = 2048) -> PagedBatch:
+    """Token-exact sparse decode at page_size=1 (sparse-paged-decode.md, issue #904).
+
+    A dense fp16 cache [batch, heads, cap, head_dim] per side is viewed, without a copy, as the
+    pool [batch*heads*cap, 1, 1, head_dim].  KV heads fold into requests (r = b*heads + h), each
+    with n_rep query heads; a request's page list is its ``selected`` sorted unique positions,
+    drawn uniformly without replacement, offset by the head stride ``cap``."""
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(batch, heads * n_rep, head_dim, generator=gen, dtype=torch.float32)
+    k = torch.empty(batch, heads, cap, head_dim, dtype=torch.float16)
+    v = torch.empty(batch, heads, cap, head_dim, dtype=torch.float16)
+    for b in range(batch):
+        for h in range(heads):
+            k[b, h] = torch.randn(cap, head_dim, generator=gen).half()
+            v[b, h] = torch.randn(cap, head_dim, generator=gen).half()
+    positions = []
+    for r in range(batch * heads):
+        pos = torch.randperm(cap, generator=gen)[:selected].sort().values
+        positions.append(pos)
+    indices = torch.cat([r * cap + p for r, p in enumerate(positions)]).to(torch.int32)
+    R = batch * heads
+    return PagedBatch(
+        name="sparse_token_exact", q=q.reshape(R, n_rep, head_dim),
+        k_pool=k.reshape(batch * heads * cap, 1, 1, head_dim),
+        v_pool=v.reshape(batch * heads * cap, 1, 1, head_dim),
+        indices=indices,
+        indptr=torch.arange(0, (R + 1) * selected, selected, dtype=torch.int32),
+        last_page_len=torch.ones(R, dtype=torch.int32),
+        first_page_offset=torch.zeros(R, dtype=torch.int32),
+        seq_lens=[selected] * R, page_size=1, num_qo_heads=n_rep, num_kv_heads=1,
+        head_dim=head_dim, scale=1.0 / math.sqrt(head_dim),
+        meta={"positions": positions, "cap": cap, "dense_shape": (batch, heads, cap, head_dim)})
+
+
+@dataclass
+class CascadeBatch:
+    """M requests sharing a whole-page prefix: the flat batch plus both cascade levels' tables."""
+
+    flat: PagedBatch
+    prefix_indices: torch.Tensor        # [shared_pages] int32, full pages
+    suffix_indices: torch.Tensor        # flat page ids of the private suffixes
+    suffix_indptr: torch.Tensor         # [M+1]
+    suffix_last_page_len: torch.Tensor  # [M]
+    suffix_lens: list[int]
+
+
+def cascade_shared_prefix(seed: int = 1004, members: int = 4, prefix_tokens: int = 8192,
+                          suffix_range: tuple[int, int] = (256, 2048), num_qo_heads: int = 32,
+                          num_kv_heads: int = 8, head_dim: int = 128, page_size: int = 16,
+                          dtype: torch.dtype = torch.float16) -> CascadeBatch:
+    """Cascade workload (cascade-attention.md, issue #903): M members share a prefix of
+    identical page ids; private suffixes of uniform length on private pages."""
+    assert prefix_tokens % page_size == 0, "the shared span is whole pages"
+    gen = torch.Generator().manual_seed(seed)
+    suffix_lens = [int(torch.randint(suffix_range[0], suffix_range[1] + 1, (1,), generator=gen))
+                   for _ in range(members)]
+    npre = prefix_tokens // page_size
+    sgeo = [page_geometry(s, 0, page_size) for s in suffix_lens]
+    total = npre + sum(p for p, _ in sgeo)
+    P = 2 * total
+    ids = torch.randperm(P, generator=gen)[:total].to(torch.int32)
+    prefix = ids[:npre]
+    suffix = ids[npre:]
+    sindptr = [0]
+    for p, _ in sgeo:
+        sindptr.append(sindptr[-1] + p)
+    flat_indices, flat_indptr = [], [0]
+    for m in range(members):
+        own = torch.cat([prefix, suffix[sindptr[m]:sindptr[m + 1]]])
+        flat_indices.append(own)
+        flat_indptr.append(flat_indptr[-1] + len(own))
+    q = torch.randn(members, num_qo_heads, head_dim, generator=gen, dtype=torch.float32)
+    k_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    v_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    lpl = torch.tensor([l for _, l in sgeo], dtype=torch.int32)
+    flat = PagedBatch(
+        name="cascade_shared_prefix", q=q, k_pool=k_pool, v_pool=v_pool,
+        indices=torch.cat(flat_indices), indptr=torch.tensor(flat_indptr, dtype=torch.int32),
+        last_page_len=lpl.clone(), first_page_offset=torch.zeros(members, dtype=torch.int32),
+        seq_lens=[prefix_tokens + s for s in suffix_lens], page_size=page_size,
+        num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+        scale=1.0 / math.sqrt(head_dim), meta={"prefix_tokens": prefix_tokens})
+    return CascadeBatch(flat=flat, prefix_indices=prefix, suffix_indices=suffix,
+                        suffix_indptr=torch.tensor(sindptr, dtype=torch.int32),
+                        suffix_last_page_len=lpl, suffix_lens=suffix_lens)
+
+
+def scatter_dense(name: str, dense_k: Sequence[torch.Tensor], dense_v: Sequence[torch.Tensor],
+                  first_page_offsets: Sequence[int], page_size: int, num_qo_heads: int,
+                  seed: int, slack: float = 2.0, order: str = "shuffled",
+                  dtype: torch.dtype = torch.float32, fill: float = float("nan")) -> PagedBatch:
+    """Write given dense per-request sequences ``[L_r, Hkv, D]`` into a paged pool.
+
+    Request r's token i is written to page entry (first_page_offset[r] + i) mod page_size of its
+    ((first_page_offset[r] + i) div page_size)-th page; every other pool entry holds ``fill``,
+    so any read outside the sequences shows up.  This is the construction the page-resolution
+    rule inverts, used to pin it from the other side.
+    """
+    gen = torch.Generator().manual_seed(seed)
+    lens = [int(k.shape[0]) for k in dense_k]
+    Hkv, D = dense_k[0].shape[1], dense_k[0].shape[2]
+    geo = [page_geometry(L, f, page_size) for L, f in zip(lens, first_page_offsets)]
+    total = sum(p for p, _ in geo)
+    P = max(1, int(math.ceil(total * slack)))
+    if order == "shuffled":
+        ids = torch.randperm(P, generator=gen)[:total]
+    elif order == "reversed":
+        ids = torch.arange(P - 1, P - 1 - total, -1)
+    else:
+        ids = torch.arange(total)
+    k_pool = torch.full((P, page_size, Hkv, D), fill, dtype=dtype)
+    v_pool = torch.full((P, page_size, Hkv, D), fill, dtype=dtype)
+    indptr = [0]
+    for r, (L, f) in enumerate(zip(lens, first_page_offsets)):
+        base = indptr[-1]
+        for i in range(L):
+            page = int(ids[base + (f + i) // page_size])
+            k_pool[page, (f + i) % page_size] = dense_k[r][i].to(dtype)
+            v_pool[page, (f + i) % page_size] = dense_v[r][i].to(dtype)
+        indptr.append(base + geo[r][0])
+    q = torch.randn(len(lens), num_qo_heads, D, generator=gen, dtype=torch.float32)
+    return PagedBatch(
+        name=name, q=q, k_pool=k_pool, v_pool=v_pool, indices=ids.to(torch.int32),
+        indptr=torch.tensor(indptr, dtype=torch.int32),
+        last_page_len=torch.tensor([l for _, l in geo], dtype=torch.int32),
+        first_page_offset=torch.tensor([f if L > 0 else 0 for L, f in zip(lens, first_page_offsets)],
+                                       dtype=torch.int32),
+        seq_lens=lens, page_size=page_size, num_qo_heads=num_qo_heads, num_kv_heads=Hkv,
+        head_dim=D, scale=1.0 / math.sqrt(D))
+
+
+WORKLOADS = {
+    "tiny_csr": tiny_csr,
+    "llama3_8b_32k": llama3_8b_32k,
+    "sliding_window_batch": sliding_window_batch,
+    "sparse_token_exact": sparse_token_exact,
+    "cascade_shared_prefix": cascade_shared_prefix,
+}
