@@ -1,0 +1,474 @@
+"""Benchmark: fused paged-attention decode v2 on GB300, one JSON line on stdout.
+
+Workload (N=1): Llama-3-8B-shaped single-sequence decode -- B=1, Hq=32, Hkv=8,
+D=128, fp16 K/V pools, page_size=16, 32768 tokens of context on a random
+permutation of a 4096-page pool; q/K/V ~ N(0,1).  A step is one pass of the
+hot path: the partial kernel over every chunk, then the merge kernel (the plan
+is built once outside the timed region, as the pages do).  Steps rotate over
+three independent input sets (3 x 128 MiB of K/V read between reuses of a set,
+more than the 126 MB L2), so every step streams its K/V from HBM.
+
+`value` is decode KV-read GB/s: K+V bytes the step must read (every visible
+token, every KV head, both sides) over the device-timed step.  `e2e` repeats
+the measurement through the public API with host buffers: every step copies q
+and the page table in from pinned host memory, checks the cached plan, runs the
+kernels and reads the output and LSE back.
+
+`--impl reference` times the f64 CPU oracle on the host cores instead (a
+deliberately slow baseline), on a bounded sample of the same workload.
+
+Multi-GPU: the path shards without any exchange (independent requests / KV
+heads), so N ranks run N independent replicas (weak scaling); value is the
+sum over ranks of bytes over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode KV-read GB/s (% of GB300 HBM peak) and µs/step at 32K context"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_v2_partial_llama3_8b_32k.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=3, help="rotating input sets (L2 avoidance)")
+    ap.add_argument("--graph", type=int, default=1, help="replay captured CUDA graphs of the steps")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--context", type=int, default=32768)
+    ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
+    ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
+    ap.add_argument("--profile", type=int, default=0,
+                    help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_src: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel changed since."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_traffic:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return int(m_traffic.group(1)) if cur == m_hash.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def summary(self):
+        import datetime
+        rows = []
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append({"t": ts, "sm": float(p[1]), "max": float(p[2]), "power": float(p[3]), "hw": p[5],
+                             "hwt": p[6], "swt": p[7], "pcap": p[8]})
+            except ValueError:
+                continue
+        t0, t1 = getattr(self, "start", None), getattr(self, "end", None)
+        if t0 is not None and t1 is not None:
+            rows = [r for r in rows if t0 <= r["t"] <= t1] or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        load = rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key] == "Active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(batch, tokens: int):
+    """The same workload cut to its first `tokens` tokens: (q, pools, table) for the oracle."""
+    import torch as T
+    ps = batch.page_size
+    pages = -(-tokens // ps)
+    lpl = tokens - (pages - 1) * ps
+    return (batch.q, batch.k_pool, batch.v_pool, batch.indices[:pages], T.tensor([0, pages], dtype=T.int32),
+            T.tensor([lpl], dtype=T.int32), T.tensor([0], dtype=T.int32), batch.scale)
+
+
+def time_oracle(batch, seconds: float, tokens: int):
+    import oracle
+    args = oracle_sample(batch, tokens)
+    oracle.attention(*oracle_sample(batch, min(tokens, 256)))  # load + warm
+    kv_bytes = tokens * batch.num_kv_heads * batch.head_dim * 2 * batch.k_pool.element_size()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention(*args)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return kv_bytes * reps / el / 1e9, reps, el, oracle.num_threads()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_attention_decode_gb300 import workloads as W
+    batch = W.llama3_8b_32k(context=args.context)
+    import oracle
+    # size one step so that warmup + steps fit in about two minutes
+    probe_tokens = 2048
+    oracle.attention(*oracle_sample(batch, 64))
+    t0 = time.perf_counter()
+    oracle.attention(*oracle_sample(batch, probe_tokens))
+    per_tok = (time.perf_counter() - t0) / probe_tokens
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(16, min(args.context, budget / max(per_tok, 1e-12))))
+    sample = oracle_sample(batch, tokens)
+    for _ in range(args.warmup):
+        oracle.attention(*sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(*sample)
+    el = time.perf_counter() - t0
+    kv_bytes = tokens * batch.num_kv_heads * batch.head_dim * 2 * batch.k_pool.element_size()
+    gbs = kv_bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama3_8b_32k", "batch": 1, "num_qo_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+                   "page_size": 16, "context": args.context, "kv_dtype": "f16",
+                   "sample_tokens": tokens},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: the first {tokens} of {args.context} context tokens, all 32 heads"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU path
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    import numpy as np  # noqa: F401
+    from paged_attention_decode_gb300 import build as pa_build
+    from paged_attention_decode_gb300 import pa_v2 as pa
+    from paged_attention_decode_gb300 import workloads as W
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    pa_build.build()
+
+    # inputs (CPU, seeded) -- rank r uses seeds offset by r so replicas are independent
+    if args.profile:
+        args.sets, args.no_cpu_baseline = 1, True
+    sets_cpu = [W.llama3_8b_32k(seed=1001 + 100 * s + 10000 * rank, context=args.context)
+                for s in range(args.sets)]
+    b0 = sets_cpu[0]
+
+    # the oracle baseline on rank 0 before any GPU work
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, reps, el, cores = time_oracle(b0, args.cpu_seconds, args.context)
+        cpu_baseline = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                        "sample": f"the full step ({args.context} tokens x 32 heads) repeated {reps} times "
+                                  f"in {el:.1f} s"}
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dt = pa.KV_DTYPES[b0.dtype]
+    target = args.target or pa.pa_v2_default_target_ctas(b0.num_qo_heads, b0.num_kv_heads, b0.head_dim,
+                                                         b0.page_size, dt)
+    plan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size, b0.num_qo_heads,
+                         b0.num_kv_heads, b0.head_dim, dt, target, 0, b0.seq_lens)
+    plan.struct.kernel = args.kernel
+    ri, ti, oi = plan.device_arrays(dev)
+    sets = [b.to(dev) for b in sets_cpu]
+    N, Hq, D, B = plan.num_chunks, b0.num_qo_heads, b0.head_dim, b0.batch
+    wv = torch.empty(N, Hq, D, device=dev)
+    wl = torch.empty(N, Hq, device=dev)
+    out = torch.empty(B, Hq, D, device=dev)
+    lse = torch.empty(B, Hq, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    kv_bytes = b0.kv_bytes()
+    # partial kernel's algorithmic bytes: K/V + q + page ids + chunk arrays + its partial outputs
+    partial_bytes = (kv_bytes + b0.q.numel() * 4 + b0.indices.numel() * 4 + N * 8
+                     + N * Hq * (D + 1) * 4)
+
+    def step(i, ev=None):
+        d = sets[i % len(sets)]
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                d.first_page_offset, b0.scale, wv, wl, None, stream, ri, ti)
+        if ev is not None:
+            ev[1].record(stream)
+        if plan.needs_merge:
+            pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
+
+    launches_per_step = 1 + int(plan.needs_merge)
+
+    if args.profile:
+        with torch.cuda.stream(stream):
+            for i in range(args.profile):
+                step(i)
+        stream.synchronize()
+        print(f"profile mode: {args.profile} steps, plan ppc={plan.pages_per_chunk} chunks={N} "
+              f"ctas={plan.total_ctas}", flush=True)
+        return
+
+    # correctness guard before timing: the arms must agree with the oracle on set 0
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    import oracle
+    ref_o, ref_l = oracle.attention(*oracle_sample(b0, args.context))
+    o_now = (out if plan.needs_merge else wv[:B]).cpu().double().numpy()
+    err = float(abs(o_now - ref_o).max())
+    if err > 2e-3:
+        raise SystemExit(f"bench: GPU output disagrees with the oracle (max|d| = {err:.3e}); refusing to time")
+
+    graph = None
+    G = len(sets) * 10
+    if args.graph:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                step(i)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(G):
+                step(i)
+
+    def run_steps(k, start=0):
+        if graph is None:
+            with torch.cuda.stream(stream):
+                for i in range(k):
+                    step(start + i)
+            return
+        full, rem = divmod(k, G)
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                step(i)
+
+    # warmup
+    run_steps(args.warmup)
+    stream.synchronize()
+
+    # timed region
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        clocks.mark("start")
+        t_start.record(stream)
+        run_steps(args.steps)
+        t_end.record(stream)
+        stream.synchronize()
+        clocks.mark("end")
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    # per-launch duration of the dominant (partial) kernel: event pairs on its stream,
+    # eager launches over the same rotating inputs
+    n_ev = 300
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)   # keep the GPU busy while the host enqueues every launch
+        for i in range(n_ev):
+            step(i, evs[i])
+    stream.synchronize()
+    partial_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
+
+    peak, peak_kind = measured_peak()
+    gbs = kv_bytes * world / (ms_step * 1e-3) / 1e9
+    achieved = partial_bytes / (partial_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(os.path.join(ROOT, "paged_attention_decode_gb300", "csrc",
+                                       "pa_partial_simt.cu" if args.kernel == 1 else "pa_partial_tc.cu"))
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * gbs / world / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "pct_of_nominal_8tbs": 100.0 * gbs / world / 8000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "llama3_8b_32k", "batch": B, "num_qo_heads": Hq, "num_kv_heads": b0.num_kv_heads,
+                   "head_dim": D, "page_size": b0.page_size, "context": args.context, "kv_dtype": "f16",
+                   "kv_bytes_per_step": kv_bytes, "target_ctas": target, "pages_per_chunk": plan.pages_per_chunk,
+                   "num_chunks": N, "ctas": plan.total_ctas, "merge": bool(plan.needs_merge),
+                   "l2": f"rotating {len(sets)} independent input sets ({len(sets) * kv_bytes >> 20} MiB of K/V "
+                         "between reuses of a set; L2 is 126 MB)",
+                   "cuda_graph": bool(graph is not None), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm",
+                     "kernel": "pa_v2_partial_simt_kernel" if args.kernel == 1 else "pa_v2_partial_tc_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": partial_bytes, "launch_us": partial_ms * 1e3,
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "cpu_baseline": cpu_baseline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
+    """Per step: pinned H2D of q and the page table, plan check, kernels, D2H of out + lse, sync."""
+    B, Hq, D = b0.batch, b0.num_qo_heads, b0.head_dim
+    host_in = []
+    for b in sets_cpu:
+        host_in.append([t.pin_memory() for t in (b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)])
+    dev_in = [[torch.empty_like(t, device=dev) for t in h] for h in host_in]
+    out_h = torch.empty(B, Hq, D).pin_memory()
+    lse_h = torch.empty(B, Hq).pin_memory()
+    wv = torch.empty(plan.num_chunks, Hq, D, device=dev)
+    wl = torch.empty(plan.num_chunks, Hq, device=dev)
+    out = torch.empty(B, Hq, D, device=dev)
+    lse = torch.empty(B, Hq, device=dev)
+    ri, ti, oi = plan.device_arrays(dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    def one(i):
+        k = i % len(sets)
+        hi, di = host_in[k], dev_in[k]
+        if not pa.pa_v2_plan_matches(plan, hi[2], hi[3], hi[4]):
+            raise RuntimeError("plan no longer matches")
+        with torch.cuda.stream(stream):
+            for src, dst in zip(hi, di):
+                dst.copy_(src, non_blocking=True)
+            q, idx, ip, lp, fp = di
+            pa.pa_v2_decode_partial(plan, q, sets[k].k_pool, sets[k].v_pool, idx, ip, lp, fp, b0.scale, wv, wl,
+                                    None, stream, ri, ti)
+            if plan.needs_merge:
+                pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+            else:
+                out_h.copy_(wv[:B], non_blocking=True)
+                lse_h.copy_(wl[:B], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(20):
+        one(i)
+    n = args.e2e_steps
+    t0 = time.perf_counter()
+    for i in range(n):
+        one(i)
+    el = time.perf_counter() - t0
+    kv_bytes = b0.kv_bytes()
+    return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pa_v2_plan_matches + pa_v2_decode_partial + pa_merge_states via the ctypes binding"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * pa_v2.h -- C ABI of libpa_v2.so: fused paged-attention decode v2 on GB300 (sm_103a).
+ *
+ * Three calls make one decode step, as the problem statement lays them out
+ * (issue #898 "Fused paged-attention decode v2: CSR page table, cross-CTA
+ * split-KV, and variable-length merge kernels", design pieces 1-4 and Task
+ * 2-4; PR #984 "fused paged-attention decode v2 with CSR page table and
+ * cross-CTA split-KV", What changed 2-5):
+ *
+ *   pa_v2_plan            host: validate the CSR geometry, choose the chunk size
+ *                         and emit the flat chunk index arrays (plain data,
+ *                         reusable across steps).
+ *   pa_v2_decode_partial  device: one CTA per (chunk, kv head, q-head group)
+ *                         writes each chunk's normalized partial output and
+ *                         its base-2 log-sum-exp.
+ *   pa_merge_states       device: variable-length merge of (V, LSE) rows grouped
+ *                         by o_indptr.  Skipped when plan.needs_merge == 0: the
+ *                         partial output is then already the answer.
+ *
+ * Conventions for every call:
+ *  - Ownership.  The library allocates no device memory and keeps no pointer
+ *    after a call returns.  Every buffer belongs to the caller; the plan
+ *    states the partial-workspace sizes up front.
+ *  - Errors.  Calls return a pa_status; nothing is printed and nothing is
+ *    thrown.  Arguments are validated on the host before any launch; a
+ *    rejected call launches nothing.  Launch failures return PA_ECUDA.
+ *  - Device-side checks.  Device index arrays cannot be validated on the
+ *    host.  The kernels bounds-check every page slot, page id and o_indptr
+ *    entry they read; an out-of-range value is skipped (its loads are not
+ *    issued) and, when the caller passes a status word, recorded there by
+ *    OR-ing PA_DEVICE_* bits.  The status word is read by the caller after
+ *    the stream has synchronized.
+ *  - Streams.  Device calls are asynchronous on the given cudaStream_t
+ *    (passed as void*; NULL is the legacy default stream).
+ *  - Units.  Every LSE is in log2 units (scores run in base 2 with log2(e)
+ *    folded into the scale); the natural-log LSE is lse2 * ln 2.
+ *  - Layouts are row-major and contiguous:
+ *      q            [batch, num_qo_heads, head_dim]              float32
+ *      k_pool/v_pool [num_pages, page_size, num_kv_heads, head_dim] kv_dtype
+ *      indices      [indptr[batch]] int32 physical page ids
+ *      indptr       [batch + 1]     int32 prefix sums of pages per request
+ *      last_page_len, first_page_offset [batch] int32
+ *    Query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ */
+#ifndef PA_V2_H
+#define PA_V2_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_EINVAL = -1,        /* a null pointer, a negative size or a misaligned buffer */
+    PA_EGEOMETRY = -2,     /* the CSR page table breaks the geometry rules */
+    PA_ECAPACITY = -3,     /* caller's chunk arrays too small; plan->num_chunks holds the need */
+    PA_EUNSUPPORTED = -4,  /* a head_dim / dtype / page_size the kernels do not serve */
+    PA_ECUDA = -5,         /* a CUDA runtime call or a launch failed */
+    PA_EOOB = -6           /* device-side out-of-range data (see pa_status_from_device) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Device status bits (OR-ed into the optional status word). */
+#define PA_DEVICE_BAD_REQUEST   0x1  /* request_indices entry outside [0, batch) */
+#define PA_DEVICE_BAD_SLOT      0x2  /* a page slot outside [0, num_indices) */
+#define PA_DEVICE_BAD_PAGE      0x4  /* a page id outside [0, num_pages) */
+#define PA_DEVICE_BAD_INDPTR    0x8  /* o_indptr decreasing or outside [0, num_partials] */
+#define PA_DEVICE_WAIT_TIMEOUT  0x10 /* a bounded wait for staged K/V gave up */
+
+/* Largest chunk count of any plan: the 65535 grid-z bound of the pages'
+ * launch shape (PR #984, What changed 4), kept as a plan invariant. */
+#define PA_V2_MAX_CHUNKS 65535
+
+/* The plan (PR #984, What changed 4; issue #898, design piece 4).  Plain old
+ * data: it can be copied, cached and reused across decode steps for as long
+ * as pa_v2_plan_matches() holds, i.e. until a request crosses a page
+ * boundary.  Chunk c covers page slots [t * pages_per_chunk,
+ * min((t + 1) * pages_per_chunk, pages_r)) of request r =
+ * request_indices[c], t = kv_tile_indices[c]; chunks are in request order. */
+typedef struct pa_v2_plan_t {
+    int32_t batch, num_qo_heads, num_kv_heads, head_dim, page_size;
+    int32_t kv_dtype;                 /* pa_dtype */
+    int32_t q_heads_per_cta, q_groups;
+    int32_t pages_per_chunk;          /* chosen chunk size in pages */
+    int32_t lo_pages_per_chunk;       /* smallest launchable size (chunk-count floor) */
+    int32_t hi_pages_per_chunk;       /* max(1, longest request in pages) */
+    int32_t num_chunks;               /* N: rows of the partial workspace */
+    int32_t needs_merge;              /* 1 iff num_chunks > batch */
+    int32_t target_ctas, total_ctas;  /* total_ctas = num_chunks * num_kv_heads * q_groups */
+    int32_t kernel;                   /* 0: tensor cores for f16/bf16 pools, CUDA cores for f32;
+                                         1: CUDA cores (needs q_heads_per_cta <= 8).  Set by the
+                                         caller after pa_v2_plan; pa_v2_plan writes 0. */
+    int64_t num_indices;              /* indptr[batch] */
+    int64_t workspace_v_bytes;        /* num_chunks * num_qo_heads * head_dim * 4 */
+    int64_t workspace_lse_bytes;      /* num_chunks * num_qo_heads * 4 */
+    uint64_t geometry_hash;           /* FNV-1a of batch and per-request page counts */
+} pa_v2_plan_t;
+
+/* Query heads one CTA serves for GQA group size `group_size`: up to 16 for
+ * f16/bf16 pools (tensor-core kernel), up to 8 for f32 pools (CUDA-core
+ * kernel).  The plan and the launcher both call this, so the CTA count and the
+ * grid cannot drift apart (PR #984, What changed 2).  Returns 0 for an
+ * unsupported shape. */
+int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype);
+
+/* Occupancy-derived CTA target for `device`: SM count times the partial
+ * kernel's resident CTAs per SM for this shape (issue #898, Task 4: "a target
+ * derived from SM count").  Writes *target_ctas. */
+pa_status pa_v2_default_target_ctas(int32_t device, int32_t num_qo_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t page_size, int32_t kv_dtype,
+                                    int32_t* target_ctas);
+
+/* Build a plan.  All pointers are HOST pointers.
+ *  indptr [batch+1], last_page_len [batch], first_page_offset [batch]: the CSR
+ *    geometry.  Checked: indptr[0] == 0 and non-decreasing; a request with
+ *    pages has 1 <= last_page_len <= page_size, 0 <= first_page_offset <
+ *    page_size, and first_page_offset < last_page_len when it has one page; a
+ *    request with no pages has last_page_len == first_page_offset == 0.
+ *  seq_lens [batch] (nullable): when given, the identity
+ *    (pages-1)*page_size + last_page_len - first_page_offset == seq_len is
+ *    checked for every request (PR #984, What changed 1).
+ *  target_ctas > 0: the CTA count to reach; pages_per_chunk_override > 0
+ *    fixes the chunk size instead of searching.
+ *  request_indices / kv_tile_indices [cap_chunks], o_indptr [batch+1]: outputs.
+ * Returns PA_EGEOMETRY on a bad table, PA_EUNSUPPORTED for a shape the
+ * kernels do not serve, PA_EINVAL when no chunk size keeps the chunk count
+ * within PA_V2_MAX_CHUNKS, and PA_ECAPACITY (with out->num_chunks set) when
+ * cap_chunks is too small.  Always sufficient: cap_chunks >=
+ * sum_r max(1, pages_r). */
+pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len,
+                     const int32_t* first_page_offset, const int32_t* seq_lens, int32_t batch,
+                     int32_t page_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t kv_dtype, int32_t target_ctas,
+                     int32_t pages_per_chunk_override, int32_t* request_indices,
+                     int32_t* kv_tile_indices, int32_t cap_chunks, int32_t* o_indptr,
+                     pa_v2_plan_t* out);
+
+/* 1 if `plan` is still valid for this geometry (same batch and per-request
+ * page counts, and a geometry that passes the checks of pa_v2_plan); else 0.
+ * Host pointers. */
+int32_t pa_v2_plan_matches(const pa_v2_plan_t* plan, const int32_t* indptr,
+                           const int32_t* last_page_len, const int32_t* first_page_offset,
+                           int32_t batch);
+
+/* The partial kernel (issue #898, design piece 2 and Task 2; PR #984, What
+ * changed 2).  One CTA per (chunk, kv head, q-head group) walks the chunk's
+ * pages through the CSR table, reads every K/V element once for all query
+ * heads of its group, runs an online softmax in base 2 in f32 and writes
+ *   v_out   [num_chunks, num_qo_heads, head_dim] f32: the chunk's normalized output
+ *   lse2_out [num_chunks, num_qo_heads]          f32: its log2-LSE
+ * An empty chunk (a request with no visible token) writes zeros and -inf.
+ * When plan->needs_merge == 0 these rows are the final output, one per
+ * request.  All array pointers are DEVICE pointers; `plan` is a host pointer.
+ * Alignment: pools, q, v_out 16-byte aligned.  num_pages: pool pages
+ * (num_pages * page_size < 2^31).  num_indices: length of `indices`.
+ * status: nullable device int32 receiving PA_DEVICE_* bits.
+ * Supported: head_dim 64 or 128; kv_dtype f32, f16, bf16; page_size 1..16 or
+ * a multiple of 16 up to 256. */
+pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
+                               const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                               const int32_t* indices, int64_t num_indices, const int32_t* indptr,
+                               const int32_t* last_page_len, const int32_t* first_page_offset,
+                               const int32_t* request_indices, const int32_t* kv_tile_indices,
+                               float sm_scale, float* v_out, float* lse2_out, int32_t* status,
+                               void* cuda_stream);
+
+/* The variable-length merge (issue #898, design piece 3 and Task 3; PR
+ * #984, What changed 3).  For output row r and head h, the rows
+ * o_indptr[r] .. o_indptr[r+1]-1 of (v_in, lse2_in) merge by
+ *   m = max lse_i, w_i = 2^(lse_i - m),
+ *   v_out = sum w_i v_i / sum w_i, lse2_out = log2(sum w_i) + m.
+ * A -inf row contributes nothing; a group with no finite row (or no row)
+ * gives zeros and -inf.  It knows nothing about paging, so any grouping of
+ * contiguous rows works (cascade composition reuses it unchanged).
+ *   v_in [num_partials, num_heads, head_dim] f32, lse2_in [num_partials, num_heads] f32,
+ *   o_indptr [num_rows_out + 1] int32, v_out [num_rows_out, num_heads, head_dim] f32,
+ *   lse2_out [num_rows_out, num_heads] f32.
+ * DEVICE pointers; v_in / v_out 16-byte aligned.  status as above. */
+pa_status pa_merge_states(const float* v_in, const float* lse2_in, const int32_t* o_indptr,
+                          int32_t num_rows_out, int32_t num_partials, int32_t num_heads,
+                          int32_t head_dim, float* v_out, float* lse2_out, int32_t* status,
+                          void* cuda_stream);
+
+/* Map a device status word (PA_DEVICE_* bits) to a pa_status: 0 -> PA_OK,
+ * a wait timeout -> PA_ECUDA, any out-of-range bit -> PA_EOOB. */
+pa_status pa_status_from_device(int32_t status_word);
+
+/* Human-readable name of a pa_status value (static storage). */
+const char* pa_status_string(int32_t status);
+
+/* Library version string (static storage). */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_V2_H */

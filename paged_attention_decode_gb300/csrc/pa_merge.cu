@@ -1,0 +1,154 @@
+// pa_merge.cu -- the variable-length merge-state kernel and its C-ABI launcher.
+//
+// Issue #898 ("Fused paged-attention decode v2: CSR page table, cross-CTA
+// split-KV, and variable-length merge kernels"), design piece 3, and PR #984
+// ("fused paged-attention decode v2 with CSR page table and cross-CTA
+// split-KV"), What changed 3: partial attention states (v_i, lse_i), each v_i
+// already normalized and lse_i in log2 units, combine by
+//   m = max lse_i, w_i = 2^(lse_i - m), v = sum w_i v_i / sum w_i,
+//   lse = log2(sum w_i) + m
+// over the rows o_indptr[r] .. o_indptr[r+1]-1 of output row r.  -inf rows
+// weigh 0; a group without a finite row yields zeros and -inf.  One row is an
+// exact identity (w = 1).
+//
+// Layout on sm_103a: the merge reads little data (the partial workspace) and
+// is bound by memory latency, so it is organised to keep many independent
+// loads in flight.  One CTA of 4 warps per (output row, head): the CTA takes
+// the group's max LSE in one round of loads, then each warp walks a quarter of
+// the group's rows with 128-bit loads (4 head-dim floats per lane) unrolled 8
+// deep, and the warps' sums meet in shared memory.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_v2.h"
+
+namespace pa {
+namespace {
+
+constexpr int kMergeWarps = 4;
+constexpr int kMergeUnroll = 8;
+
+__device__ __forceinline__ float merge_weight(float l, float m) {
+  return l == -INFINITY ? 0.f : fast_exp2(l - m);
+}
+
+// VECTOR: head_dim % 4 == 0 and head_dim <= 128 (one float4 per lane); else a
+// scalar loop over head_dim.
+template <bool VECTOR>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    pa_merge_states_kernel(const float* __restrict__ v_in, const float* __restrict__ lse_in,
+                           const int32_t* __restrict__ o_indptr, int32_t num_rows_out, int32_t num_partials,
+                           int32_t num_heads, int32_t head_dim, float* __restrict__ v_out,
+                           float* __restrict__ lse_out, int32_t* status) {
+  __shared__ float red[kMergeWarps];
+  __shared__ float wsum_s[kMergeWarps];
+  __shared__ __align__(16) float acc_s[kMergeWarps][128];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x / num_heads;
+  const int h = blockIdx.x % num_heads;
+  int i0 = o_indptr[r];
+  int i1 = o_indptr[r + 1];
+  if (i0 < 0 || i1 < i0 || i1 > num_partials) {
+    if (threadIdx.x == 0) report(status, PA_DEVICE_BAD_INDPTR);
+    i0 = i1 = 0;
+  }
+  const size_t hs = (size_t)num_heads;
+
+  // group max of the LSEs
+  float m = -INFINITY;
+  for (int i = i0 + threadIdx.x; i < i1; i += kMergeWarps * 32) m = fmaxf(m, lse_in[i * hs + h]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, red[w]);
+
+  float* out = v_out + ((size_t)r * num_heads + h) * head_dim;
+  if (m == -INFINITY) {
+    for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) out[d] = 0.f;
+    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = -INFINITY;
+    return;
+  }
+
+  if (VECTOR) {
+    const int d4n = head_dim >> 2;
+    const bool active = lane < d4n;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
+    // warp w takes rows i0 + w, i0 + w + 4, ...; 8 independent row loads per round
+    for (int base = i0 + warp; base < i1; base += kMergeWarps * kMergeUnroll) {
+      float l[kMergeUnroll];
+      float4 v[kMergeUnroll];
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const int i = base + u * kMergeWarps;
+        l[u] = i < i1 ? lse_in[i * hs + h] : -INFINITY;
+        v[u] = (i < i1 && active) ? reinterpret_cast<const float4*>(v_in + (i * hs + h) * head_dim)[lane]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const float w = merge_weight(l[u], m);
+        ws += w;
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
+    }
+    if (active) reinterpret_cast<float4*>(acc_s[warp])[lane] = acc;
+    if (lane == 0) wsum_s[warp] = ws;
+    __syncthreads();
+    float W = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) W += wsum_s[w];
+    for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kMergeWarps; ++w) a += acc_s[w][d];
+      out[d] = a / W;
+    }
+    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = fast_log2(W) + m;
+  } else {
+    // general head_dim: the whole CTA walks the rows, one head-dim element per thread
+    float W = 0.f;
+    for (int i = i0; i < i1; ++i) W += merge_weight(lse_in[i * hs + h], m);
+    for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) {
+      float a = 0.f;
+      for (int i = i0; i < i1; ++i) a = fmaf(merge_weight(lse_in[i * hs + h], m), v_in[(i * hs + h) * head_dim + d], a);
+      out[d] = a / W;
+    }
+    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = fast_log2(W) + m;
+  }
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, const int32_t* o_indptr,
+                                     int32_t num_rows_out, int32_t num_partials, int32_t num_heads,
+                                     int32_t head_dim, float* v_out, float* lse2_out, int32_t* status,
+                                     void* cuda_stream) {
+  if (num_rows_out < 0 || num_partials < 0 || num_heads < 1 || head_dim < 1) return PA_EINVAL;
+  if (num_rows_out == 0) return PA_OK;
+  if (!o_indptr || !v_out || !lse2_out || (num_partials > 0 && (!v_in || !lse2_in))) return PA_EINVAL;
+  const bool vec = head_dim % 4 == 0 && head_dim <= 128;
+  if (vec && (((uintptr_t)v_in | (uintptr_t)v_out) & 15u)) return PA_EINVAL;
+  const long long blocks = (long long)num_rows_out * num_heads;
+  if (blocks > 0x7fffffffLL) return PA_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (vec)
+    pa::pa_merge_states_kernel<true><<<(unsigned)blocks, pa::kMergeWarps * 32, 0, s>>>(
+        v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status);
+  else
+    pa::pa_merge_states_kernel<false><<<(unsigned)blocks, pa::kMergeWarps * 32, 0, s>>>(
+        v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+}

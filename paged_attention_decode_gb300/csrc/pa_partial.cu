@@ -1,0 +1,195 @@
+// pa_partial.cu -- C-ABI entry of the split-KV partial kernel: argument checks,
+// kernel-variant choice, TMA tensor maps over the pools, launch; the
+// q-heads-per-CTA rule; and the occupancy-derived default CTA target of the plan.
+//
+// Variants (same contract; issue #898 "Fused paged-attention decode v2: CSR
+// page table, cross-CTA split-KV, and variable-length merge kernels", design
+// piece 2; PR #984 "fused paged-attention decode v2 with CSR page table and
+// cross-CTA split-KV", What changed 2):
+//  - tensor cores (pa_partial_tc.cu) for f16 / bf16 pools, up to 16 query
+//    heads per CTA;
+//  - CUDA cores (pa_partial_simt.cu) for f32 pools (or on request through
+//    plan.kernel), up to 8 query heads per CTA.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+bool prepare_kernel(const void* fn, size_t smem) {
+  constexpr int kMaxDevices = 64;
+  constexpr int kMaxKernels = 128;
+  static std::mutex mu;
+  static const void* done[kMaxDevices][kMaxKernels] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < kMaxKernels; ++i) {
+    if (done[dev][i] == fn) return true;
+    if (done[dev][i] == nullptr) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return false;
+      done[dev][i] = fn;
+      return true;
+    }
+  }
+  return false;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a pool viewed as [rows = num_pages * page_size, Hkv, D]
+// (innermost first: D, Hkv, rows); a box is one KV head x `box_rows` rows x
+// `box_d` elements of the head dim.
+bool make_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t rows, int hkv, int D, int box_d,
+                   int box_rows, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esize = dtype == PA_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)hkv * D * esize};
+  cuuint32_t box[3] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult rc = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool use_tensor_cores(int kv_dtype, int kernel) {
+  return kernel != 1 && (kv_dtype == PA_F16 || kv_dtype == PA_BF16);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype) {
+  if (group_size < 1 || (head_dim != 64 && head_dim != 128)) return 0;
+  if (kv_dtype == PA_F16 || kv_dtype == PA_BF16) return group_size < 16 ? group_size : 16;
+  if (kv_dtype == PA_F32) return group_size < 8 ? group_size : 8;
+  return 0;
+}
+
+extern "C" pa_status pa_v2_default_target_ctas(int32_t device, int32_t num_qo_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t page_size, int32_t kv_dtype,
+                                               int32_t* target_ctas) {
+  if (!target_ctas || num_kv_heads < 1 || num_qo_heads < num_kv_heads || num_qo_heads % num_kv_heads ||
+      page_size < 1)
+    return PA_EINVAL;
+  const int hpc = pa_v2_q_heads_per_cta(num_qo_heads / num_kv_heads, head_dim, kv_dtype);
+  if (hpc == 0) return PA_EUNSUPPORTED;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return PA_ECUDA;
+  if (device != prev && cudaSetDevice(device) != cudaSuccess) return PA_ECUDA;
+  int sms = 0, per_sm = 0, rc = PA_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess) {
+    rc = pa::use_tensor_cores(kv_dtype, 0)
+             ? pa::occupancy_partial_tc(kv_dtype, head_dim, hpc, pa::tc_uses_tma(page_size), &per_sm)
+             : pa::occupancy_partial_simt(kv_dtype, head_dim, hpc, &per_sm);
+  }
+  if (device != prev) cudaSetDevice(prev);
+  if (rc != PA_OK) return (pa_status)rc;
+  if (per_sm < 1) return PA_ECUDA;
+  *target_ctas = sms * per_sm;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
+                                          const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                          const int32_t* indices, int64_t num_indices, const int32_t* indptr,
+                                          const int32_t* last_page_len, const int32_t* first_page_offset,
+                                          const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                          float sm_scale, float* v_out, float* lse2_out, int32_t* status,
+                                          void* cuda_stream) {
+  if (!plan) return PA_EINVAL;
+  if (plan->num_chunks == 0) return PA_OK;
+  if (!q || !k_pool || !v_pool || !indices || !indptr || !last_page_len || !first_page_offset ||
+      !request_indices || !kv_tile_indices || !v_out || !lse2_out)
+    return PA_EINVAL;
+  if (kv_dtype != plan->kv_dtype || num_pages < 1 || num_indices < plan->num_indices || plan->num_chunks < 0 ||
+      plan->num_kv_heads < 1 || plan->q_groups < 1 || plan->page_size < 1 || !std::isfinite(sm_scale))
+    return PA_EINVAL;
+  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) || !pa::aligned16(v_out))
+    return PA_EINVAL;
+  const int D = plan->head_dim;
+  const int ps = plan->page_size;
+  if (num_pages * (int64_t)ps >= (1ll << 31)) return PA_EUNSUPPORTED;
+  const int hpc = pa_v2_q_heads_per_cta(plan->num_qo_heads / plan->num_kv_heads, D, kv_dtype);
+  if (hpc != plan->q_heads_per_cta) return PA_EINVAL;
+  const bool tc = pa::use_tensor_cores(kv_dtype, plan->kernel);
+  if (!tc && hpc > 8) return PA_EUNSUPPORTED;
+  const bool tma = !tc || pa::tc_uses_tma(ps);
+
+  alignas(64) CUtensorMap tm_k, tm_v;
+  std::memset(&tm_k, 0, sizeof(tm_k));
+  std::memset(&tm_v, 0, sizeof(tm_v));
+  if (tma) {
+    const int box_rows = ps <= pa::kStageRows ? ps : pa::kStageRows;
+    const int box_d = tc ? 64 : D;
+    const CUtensorMapSwizzle sw = tc ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (!pa::make_pool_map(&tm_k, k_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw) ||
+        !pa::make_pool_map(&tm_v, v_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw))
+      return PA_ECUDA;
+  }
+
+  pa::LaunchArgs a;
+  pa::PartialParams& p = a.p;
+  p.q = q;
+  p.indices = indices;
+  p.indptr = indptr;
+  p.last_page_len = last_page_len;
+  p.first_page_offset = first_page_offset;
+  p.request_indices = request_indices;
+  p.kv_tile_indices = kv_tile_indices;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.v_out = v_out;
+  p.lse_out = lse2_out;
+  p.status = status;
+  p.num_pages = num_pages;
+  p.num_indices = num_indices;
+  p.batch = plan->batch;
+  p.num_qo_heads = plan->num_qo_heads;
+  p.num_kv_heads = plan->num_kv_heads;
+  p.group = plan->num_qo_heads / plan->num_kv_heads;
+  p.hpc = hpc;
+  p.q_groups = plan->q_groups;
+  p.page_size = ps;
+  p.pages_per_chunk = plan->pages_per_chunk;
+  const pa::FastDiv fd = pa::FastDiv::make((uint32_t)ps);
+  p.ps_magic = fd.magic;
+  p.ps_shift = fd.shift;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  a.kv_dtype = kv_dtype;
+  a.head_dim = D;
+  a.num_chunks = plan->num_chunks;
+  a.stream = static_cast<cudaStream_t>(cuda_stream);
+  return (pa_status)(tc ? pa::launch_partial_tc(a, tma) : pa::launch_partial_simt(a));
+}

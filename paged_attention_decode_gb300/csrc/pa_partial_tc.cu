@@ -1,0 +1,545 @@
+// pa_partial_tc.cu -- tensor-core variant of the split-KV partial kernel (f16 / bf16 pools).
+//
+// Same contract as the CUDA-core variant (issue #898 "Fused paged-attention
+// decode v2: CSR page table, cross-CTA split-KV, and variable-length merge
+// kernels", design pieces 1-2; PR #984 "fused paged-attention decode v2 with
+// CSR page table and cross-CTA split-KV", What changed 2): one CTA per (chunk,
+// kv head, q-head group), each K/V element read once for the whole group, an
+// online softmax in base 2, a normalized partial and its log2-LSE per chunk.
+//
+// Why tensor cores here.  Decode attention is HBM-bound, but with a GQA group
+// of 4-16 heads a CUDA-core mapping spends ~1.5k warp instructions per 16
+// tokens on FMAs, conversions and shuffle reductions, which keeps the SM
+// issue-bound below the HBM roofline.  Per 16-token stage this kernel instead
+// issues two m16n8k16 MMAs per 16 head-dims for Q.K and two per 16 head-dims
+// for P.V (warp-level mma.sync), each fed by one ldmatrix:
+//
+//   S^T [16 tokens x 8 heads] = K [16 x D] . Q^T [D x 8]          (tokens are M)
+//   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]
+//
+// The K/V stage is 16 rows of one KV head stored as 128-byte half rows with
+// the 16-byte chunk index XOR-ed by (row mod 8) -- the layout TMA's 128-byte
+// swizzle writes -- so every ldmatrix phase touches 8 distinct bank groups.
+// Q and P enter the MMA as hi + lo pairs of the pool's 16-bit type (x = hi +
+// lo with hi = round(x), lo = round(x - hi)): products of the exact 16-bit K/V
+// values with both halves accumulate in f32, which keeps the scores and the
+// output at f32-level accuracy instead of the 2^-9 (bf16) rounding of a single
+// 16-bit operand.
+//
+// Staging: TMA (cp.async.bulk.tensor with SWIZZLE_128B, completion on an
+// mbarrier) when pages start on 8-row boundaries of a stage (page_size 8, 16
+// or a multiple of 16); otherwise cp.async 16-byte copies that apply the same
+// swizzle in the destination address, with the row -> (page, entry) split done
+// by a fast division by page_size.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+// ---- 16-bit element type traits -------------------------------------------
+
+template <typename T> struct TC;
+
+template <> struct TC<__half> {
+  __device__ __forceinline__ static float round(float x) { return __half2float(__float2half_rn(x)); }
+  __device__ __forceinline__ static uint32_t pack(float lo16, float hi16) {
+    __half2 h = __floats2half2_rn(lo16, hi16);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static unsigned short bits(float x) {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<unsigned short*>(&h);
+  }
+  __device__ __forceinline__ static void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+template <> struct TC<__nv_bfloat16> {
+  __device__ __forceinline__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+  __device__ __forceinline__ static uint32_t pack(float lo16, float hi16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo16, hi16);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static unsigned short bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<unsigned short*>(&h);
+  }
+  __device__ __forceinline__ static void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Byte offset of 16-byte chunk `ch` (0 .. D/8-1) of stage row `row` in a
+// swizzled tile: 128-byte half rows, half-tiles of 16 rows (2 KB) each, chunk
+// index XOR (row mod 8) within the half row.
+__device__ __forceinline__ uint32_t swz(int row, int ch) {
+  return (uint32_t)((ch >> 3) * 2048 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// ---- the kernel -------------------------------------------------------------
+
+template <int D, int NT, int NSW>
+struct TcLayout {
+  static constexpr int HP = 8 * NT;                 // query heads per CTA (padded)
+  static constexpr int TILE = (D / 64) * 2048;       // bytes of one side of a stage
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int STAGES_BYTES = kWarps * NSW * STAGE;
+  static constexpr int PT_BYTES = kWarps * 2 * HP * 32;   // P^T hi/lo per warp: [HP][16] 16-bit
+  static constexpr int STATE_BYTES = kWarps * HP * D * 4;
+  static constexpr int BODY = STAGES_BYTES > STATE_BYTES ? STAGES_BYTES : STATE_BYTES;
+  static constexpr int BARS = BODY + PT_BYTES;
+  static constexpr int MS = BARS + kWarps * NSW * 8;
+  static constexpr int TOTAL = MS + 2 * kWarps * HP * 4;
+  static constexpr int ALLOC = TOTAL + 1024;         // room to align the base to 1 KB
+};
+
+// T: __half or __nv_bfloat16.  D: 64 or 128.  NT: 8-head n-tiles per CTA (1 or
+// 2).  NSW: stage ring depth per warp.  USE_TMA: staging mechanism.
+template <typename T, int D, int NT, int NSW, bool USE_TMA>
+__global__ void __launch_bounds__(kWarps * 32)
+    pa_v2_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const PartialParams p) {
+  using L = TcLayout<D, NT, NSW>;
+  constexpr int HP = L::HP;
+  constexpr int KSTEPS = D / 16;
+  constexpr int CPR = D / 8;  // 16-byte chunks per K/V row
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BARS);
+  float* ms = reinterpret_cast<float*>(smem + L::MS);
+  float* ls = ms + kWarps * HP;
+  float* accs = reinterpret_cast<float*>(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // MMA group row
+  const int t = lane & 3;   // MMA thread-in-group
+  const int c = blockIdx.x;
+  const int kvh = blockIdx.y / p.q_groups;
+  const int qg = blockIdx.y % p.q_groups;
+  const int h_first = kvh * p.group + qg * p.hpc;
+  const int nheads = min(p.hpc, p.group - qg * p.hpc);
+  const int ps = p.page_size;
+
+  int r;
+  const ChunkGeom gm = chunk_geom(p, c, &r);
+
+  unsigned char* mst = smem + warp * NSW * L::STAGE;
+  unsigned short* pt_hi = reinterpret_cast<unsigned short*>(smem + L::BODY + warp * 2 * HP * 32);
+  unsigned short* pt_lo = pt_hi + HP * 16;
+  uint64_t* mybar = bars + warp * NSW;
+  const uint64_t policy = policy_evict_first();
+  const int box_rows = ps <= kStageRows ? ps : kStageRows;
+
+  if (USE_TMA) {
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < NSW; ++s) mbar_init(&mybar[s], 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+  }
+
+  // ---- Q fragments: B operand of S^T = K Q^T, base-2 scaled, split hi + lo ----
+  uint32_t qh[KSTEPS][NT][2], ql[KSTEPS][NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int head = 8 * j + g;
+    const bool ok = head < nheads;
+    const float* qp = p.q + ((size_t)r * p.num_qo_heads + h_first + (ok ? head : 0)) * D + 2 * t;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      float x[4];
+      x[0] = ok ? qp[16 * kk] * p.scale_log2 : 0.f;
+      x[1] = ok ? qp[16 * kk + 1] * p.scale_log2 : 0.f;
+      x[2] = ok ? qp[16 * kk + 8] * p.scale_log2 : 0.f;
+      x[3] = ok ? qp[16 * kk + 9] * p.scale_log2 : 0.f;
+      float h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = TC<T>::round(x[e]);
+        l[e] = x[e] - h[e];
+      }
+      qh[kk][j][0] = TC<T>::pack(h[0], h[1]);
+      qh[kk][j][1] = TC<T>::pack(h[2], h[3]);
+      ql[kk][j][0] = TC<T>::pack(l[0], l[1]);
+      ql[kk][j][1] = TC<T>::pack(l[2], l[3]);
+    }
+  }
+
+  // ---- staging ----
+  // Lane (lane & 15) holds the page id of page (lane & 15) of stage j, or -1.
+  auto stage_page = [&](int j) -> int32_t {
+    if (j >= gm.n_stages) return -1;
+    const StageGeom s = stage_geom(gm, j, ps);
+    const int tp = lane & 15;
+    if (tp >= s.npages) return -1;
+    return __ldg(p.indices + gm.slot_base + s.slot + tp);
+  };
+  auto page_ok = [&](int32_t page) { return page >= 0 && (int64_t)page < p.num_pages; };
+
+  auto issue_tma = [&](int j, int slot, int32_t my_page) {
+    const StageGeom s = stage_geom(gm, j, ps);
+    constexpr int HALVES = D / 64;
+    const int nops = s.npages * HALVES * 2;
+    const int tp = lane / (2 * HALVES);
+    const int32_t page = __shfl_sync(0xffffffffu, my_page, tp & 15);
+    uint64_t* bar = &mybar[slot];
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nops * box_rows * 128));
+    __syncwarp();
+    if (lane < nops) {
+      const int side = (lane / HALVES) & 1;
+      const int half = lane % HALVES;
+      int row = (int)(p.num_pages * ps);  // past the pool's end: TMA zero-fills
+      if (page_ok(page)) row = page * ps + s.row0;
+      else report(p.status, PA_DEVICE_BAD_PAGE);
+      unsigned char* dst = mst + slot * L::STAGE + side * L::TILE + half * 2048 + tp * box_rows * 128;
+      tma_load_3d(dst, side ? &tm_v : &tm_k, bar, half * 64, kvh, row, policy);
+    }
+  };
+
+  auto issue_cpasync = [&](int j, int slot, int32_t my_page) {
+    const StageGeom s = stage_geom(gm, j, ps);
+    const int nrows = s.npages * ps;
+    constexpr int RSTEP = 32 / CPR;
+    const int ch = lane % CPR;
+    const int r0 = lane / CPR;
+    const uint32_t kdst = smem_addr(mst + slot * L::STAGE);
+    const uint32_t vdst = kdst + L::TILE;
+    const T* kp = static_cast<const T*>(p.k_pool);
+    const T* vp = static_cast<const T*>(p.v_pool);
+#pragma unroll
+    for (int i = 0; i < kStageRows / RSTEP; ++i) {
+      const int row = r0 + i * RSTEP;
+      const int sl = (int)fast_div((uint32_t)row, p.ps_magic, p.ps_shift);  // row / page_size
+      const int e = row - sl * ps;
+      const int32_t page = __shfl_sync(0xffffffffu, my_page, sl & 15);
+      if (row < nrows) {
+        if (page_ok(page)) {
+          const size_t elem = (((size_t)page * ps + e) * p.num_kv_heads + kvh) * D + ch * 8;
+          const uint32_t off = swz(row, ch);
+          cp_async_16(kdst + off, kp + elem, policy);
+          cp_async_16(vdst + off, vp + elem, policy);
+        } else {
+          report(p.status, PA_DEVICE_BAD_PAGE);
+        }
+      }
+    }
+  };
+
+  auto issue = [&](int j, int slot, int32_t my_page) {
+    if (USE_TMA) issue_tma(j, slot, my_page);
+    else issue_cpasync(j, slot, my_page);
+  };
+
+#pragma unroll
+  for (int s = 0; s < NSW; ++s) {
+    const int j = warp + s * kWarps;
+    if (j < gm.n_stages) issue(j, s, stage_page(j));
+    if (!USE_TMA) cp_async_commit();
+  }
+  int32_t next_page = stage_page(warp + NSW * kWarps);
+
+  float o[KSTEPS][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    m_run[j][0] = m_run[j][1] = -INFINITY;
+    l_run[j][0] = l_run[j][1] = 0.f;
+  }
+  bool failed = false;
+
+  int i = 0;
+  for (;; ++i) {
+    const int j = warp + i * kWarps;
+    if (j >= gm.n_stages) break;
+    const int slot = i % NSW;
+    if (USE_TMA) {
+      if (!mbar_wait_bounded(&mybar[slot], (i / NSW) & 1, kWaitLimitCycles)) {
+        failed = true;
+        break;
+      }
+    } else {
+      cp_async_wait<NSW - 1>();
+      __syncwarp();
+    }
+    const StageGeom sg = stage_geom(gm, j, ps);
+    unsigned char* kt = mst + slot * L::STAGE;
+    unsigned char* vt = kt + L::TILE;
+    const uint32_t kbase = smem_addr(kt);
+    const uint32_t vbase = smem_addr(vt);
+
+    // ---- S^T = K . Q^T (hi and lo halves in separate accumulators) ----
+    float sh[NT][4], sl[NT][4];
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sh[jj][e] = sl[jj][e] = 0.f;
+    {
+      const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        const int chunk = kk * 2 + (lane >> 4);
+        uint32_t a[4];
+        ldsm_x4(a, kbase + swz(row, chunk));
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj) {
+          TC<T>::mma(sh[jj], a, qh[kk][jj][0], qh[kk][jj][1]);
+          TC<T>::mma(sl[jj], a, ql[kk][jj][0], ql[kk][jj][1]);
+        }
+      }
+    }
+
+    // ---- online softmax over the stage (tokens g and g + 8, heads 2t, 2t + 1) ----
+    const bool v0 = g >= sg.lo && g < sg.hi;
+    const bool v1 = g + 8 >= sg.lo && g + 8 < sg.hi;
+    float pr[NT][4];
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      float s0 = v0 ? sh[jj][0] + sl[jj][0] : -INFINITY;
+      float s1 = v0 ? sh[jj][1] + sl[jj][1] : -INFINITY;
+      float s2 = v1 ? sh[jj][2] + sl[jj][2] : -INFINITY;
+      float s3 = v1 ? sh[jj][3] + sl[jj][3] : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run[jj][0], mx0), mn1 = fmaxf(m_run[jj][1], mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float a0 = fast_exp2(m_run[jj][0] - mu0), a1 = fast_exp2(m_run[jj][1] - mu1);
+      m_run[jj][0] = mn0;
+      m_run[jj][1] = mn1;
+      pr[jj][0] = fast_exp2(s0 - mu0);
+      pr[jj][1] = fast_exp2(s1 - mu1);
+      pr[jj][2] = fast_exp2(s2 - mu0);
+      pr[jj][3] = fast_exp2(s3 - mu1);
+      l_run[jj][0] = l_run[jj][0] * a0 + pr[jj][0] + pr[jj][2];
+      l_run[jj][1] = l_run[jj][1] * a1 + pr[jj][1] + pr[jj][3];
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        o[mt][jj][0] *= a0;
+        o[mt][jj][1] *= a1;
+        o[mt][jj][2] *= a0;
+        o[mt][jj][3] *= a1;
+      }
+      // P^T [head][token] for the B operand, hi and lo
+      const int h0 = 8 * jj + 2 * t;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hh = h0 + (e & 1);
+        const int tok = g + (e >> 1) * 8;
+        const float hi = TC<T>::round(pr[jj][e]);
+        pt_hi[hh * 16 + tok] = TC<T>::bits(hi);
+        pt_lo[hh * 16 + tok] = TC<T>::bits(pr[jj][e] - hi);
+      }
+    }
+
+    // rows of the V tile outside [lo, hi) may hold stale or non-finite data: zero them
+    if (sg.lo > 0 || sg.hi < kStageRows) {
+      for (int idx = lane; idx < kStageRows * CPR; idx += 32) {
+        const int row = idx / CPR;
+        if (row < sg.lo || row >= sg.hi)
+          *reinterpret_cast<uint4*>(vt + (idx % CPR >> 3) * 2048 + row * 128 + (idx % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    __syncwarp();
+
+    // ---- O^T += V^T . P^T ----
+    uint32_t bph[NT][2], bpl[NT][2];
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      const unsigned short* src = (lane >> 4) ? pt_lo : pt_hi;
+      const int head = 8 * jj + (lane & 7);
+      const int tokoff = ((lane >> 3) & 1) * 8;
+      uint32_t b[4];
+      ldsm_x4(b, smem_addr(src + head * 16 + tokoff));
+      bph[jj][0] = b[0];
+      bph[jj][1] = b[1];
+      bpl[jj][0] = b[2];
+      bpl[jj][1] = b[3];
+    }
+    {
+      const int tok = (lane >> 4) * 8 + (lane & 7);
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        const int chunk = mt * 2 + ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldsm_x4_trans(a, vbase + swz(tok, chunk));
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj) {
+          TC<T>::mma(o[mt][jj], a, bph[jj][0], bph[jj][1]);
+          TC<T>::mma(o[mt][jj], a, bpl[jj][0], bpl[jj][1]);
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- refill this slot with the warp's stage NSW rounds ahead ----
+    const int jn = warp + (i + NSW) * kWarps;
+    if (jn < gm.n_stages) {
+      if (USE_TMA) fence_proxy_async_smem();
+      issue(jn, slot, next_page);
+      next_page = stage_page(jn + kWarps);
+    }
+    if (!USE_TMA) cp_async_commit();
+  }
+
+  if (USE_TMA) {
+    if (failed) {
+      if (lane == 0) report(p.status, PA_DEVICE_WAIT_TIMEOUT);
+      for (int k = i + 1; k < i + NSW; ++k) {
+        if (warp + k * kWarps >= gm.n_stages) break;
+        mbar_wait_bounded(&mybar[k % NSW], (k / NSW) & 1, kWaitLimitCycles);
+      }
+    }
+  } else {
+    cp_async_wait<0>();
+  }
+
+  // ---- per-warp state -> shared memory, then merge the warps ----
+#pragma unroll
+  for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) l_run[jj][e] += __shfl_xor_sync(0xffffffffu, l_run[jj][e], off);
+  __syncthreads();  // all warps are done with their stages: reuse them for the states
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      const int h0 = 8 * jj + 2 * t;
+      float* a0 = accs + (warp * HP + h0) * D + 16 * mt + g;
+      float* a1 = a0 + D;
+      a0[0] = o[mt][jj][0];
+      a1[0] = o[mt][jj][1];
+      a0[8] = o[mt][jj][2];
+      a1[8] = o[mt][jj][3];
+    }
+  if (g == 0) {
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      const int h0 = 8 * jj + 2 * t;
+      ms[warp * HP + h0] = m_run[jj][0];
+      ms[warp * HP + h0 + 1] = m_run[jj][1];
+      ls[warp * HP + h0] = l_run[jj][0];
+      ls[warp * HP + h0 + 1] = l_run[jj][1];
+    }
+  }
+  __syncthreads();
+  combine_warps_and_store<HP, D>(p, ms, ls, accs, c, h_first, nheads);
+}
+
+// ---- host side --------------------------------------------------------------
+
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const PartialParams);
+constexpr int kTcRing = 3;
+
+struct TcInstance {
+  TcKernel fn;
+  size_t smem;
+};
+
+template <typename T, int D, int NT, bool TMA>
+TcInstance tc_make() {
+  return {pa_v2_partial_tc_kernel<T, D, NT, kTcRing, TMA>, (size_t)TcLayout<D, NT, kTcRing>::ALLOC};
+}
+
+template <typename T, int D, bool TMA>
+bool tc_pick_nt(int hpc, TcInstance* out) {
+  if (hpc <= 8) { *out = tc_make<T, D, 1, TMA>(); return true; }
+  if (hpc <= 16) { *out = tc_make<T, D, 2, TMA>(); return true; }
+  return false;
+}
+
+template <typename T, int D>
+bool tc_pick_stage(int hpc, bool tma, TcInstance* out) {
+  return tma ? tc_pick_nt<T, D, true>(hpc, out) : tc_pick_nt<T, D, false>(hpc, out);
+}
+
+bool tc_pick(int dtype, int D, int hpc, bool tma, TcInstance* out) {
+  if (dtype == PA_F16) {
+    if (D == 64) return tc_pick_stage<__half, 64>(hpc, tma, out);
+    if (D == 128) return tc_pick_stage<__half, 128>(hpc, tma, out);
+  } else if (dtype == PA_BF16) {
+    if (D == 64) return tc_pick_stage<__nv_bfloat16, 64>(hpc, tma, out);
+    if (D == 128) return tc_pick_stage<__nv_bfloat16, 128>(hpc, tma, out);
+  }
+  return false;
+}
+
+}  // namespace
+
+int launch_partial_tc(const LaunchArgs& a, bool use_tma) {
+  TcInstance inst;
+  if (!tc_pick(a.kv_dtype, a.head_dim, a.p.hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
+  if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
+  dim3 grid(a.num_chunks, a.p.num_kv_heads * a.p.q_groups);
+  inst.fn<<<grid, kWarps * 32, inst.smem, a.stream>>>(*a.tm_k, *a.tm_v, a.p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int* blocks_per_sm) {
+  TcInstance inst;
+  if (!tc_pick(kv_dtype, head_dim, hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
+  if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, inst.fn, kWarps * 32, inst.smem) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ECUDA;
+}
+
+}  // namespace pa

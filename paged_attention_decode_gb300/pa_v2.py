@@ -1,0 +1,255 @@
+"""Thin ctypes binding of libpa_v2.so (include/pa_v2.h) with the same call names.
+
+Argument marshalling only: every step of the decode path runs in the library's
+kernels.  PyTorch provides device memory and streams.  There is no fallback:
+if the library is missing or a call fails, a ``PaError`` is raised.
+
+A decode step is ``pa_v2_plan`` (host, cached across steps), then
+``pa_v2_decode_partial`` and, when ``plan.needs_merge``, ``pa_merge_states``
+(issue #898 "Fused paged-attention decode v2: CSR page table, cross-CTA
+split-KV, and variable-length merge kernels", design pieces 2-4).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa_v2.so")
+
+PA_OK, PA_EINVAL, PA_EGEOMETRY, PA_ECAPACITY, PA_EUNSUPPORTED, PA_ECUDA, PA_EOOB = 0, -1, -2, -3, -4, -5, -6
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_V2_MAX_CHUNKS = 65535
+DEVICE_BAD_REQUEST, DEVICE_BAD_SLOT, DEVICE_BAD_PAGE, DEVICE_BAD_INDPTR, DEVICE_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+
+KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+
+# Exported symbols of the C ABI (the header's declarations).
+ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
+               "pa_v2_decode_partial", "pa_merge_states", "pa_status_from_device", "pa_status_string",
+               "pa_version")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {pa_status_string(status)} ({status})")
+
+
+class PlanStruct(ctypes.Structure):
+    """Mirror of pa_v2_plan_t."""
+
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "q_heads_per_cta",
+        "q_groups", "pages_per_chunk", "lo_pages_per_chunk", "hi_pages_per_chunk", "num_chunks",
+        "needs_merge", "target_ctas", "total_ctas", "kernel")] + [
+        ("num_indices", ctypes.c_int64), ("workspace_v_bytes", ctypes.c_int64),
+        ("workspace_lse_bytes", ctypes.c_int64), ("geometry_hash", ctypes.c_uint64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa_v2.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with paged_attention_decode_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        PP = ctypes.POINTER(PlanStruct)
+        L.pa_v2_q_heads_per_cta.argtypes = [i32, i32, i32]
+        L.pa_v2_q_heads_per_cta.restype = i32
+        L.pa_v2_default_target_ctas.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
+        L.pa_v2_default_target_ctas.restype = i32
+        L.pa_v2_plan.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P, i32, P, PP]
+        L.pa_v2_plan.restype = i32
+        L.pa_v2_plan_matches.argtypes = [PP, P, P, P, i32]
+        L.pa_v2_plan_matches.restype = i32
+        L.pa_v2_decode_partial.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, f32, P, P, P, P]
+        L.pa_v2_decode_partial.restype = i32
+        L.pa_merge_states.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
+        L.pa_merge_states.restype = i32
+        L.pa_status_from_device.argtypes = [i32]
+        L.pa_status_from_device.restype = i32
+        L.pa_status_string.argtypes = [i32]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def pa_status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def pa_status_from_device(word: int) -> int:
+    return int(lib().pa_status_from_device(int(word)))
+
+
+def pa_version() -> str:
+    return lib().pa_version().decode()
+
+
+def pa_v2_q_heads_per_cta(group_size: int, head_dim: int, kv_dtype: int) -> int:
+    return int(lib().pa_v2_q_heads_per_cta(group_size, head_dim, kv_dtype))
+
+
+def pa_v2_default_target_ctas(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                              kv_dtype: int, device: int | None = None) -> int:
+    dev = torch.cuda.current_device() if device is None else device
+    out = ctypes.c_int32()
+    rc = lib().pa_v2_default_target_ctas(dev, num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype,
+                                         ctypes.byref(out))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_default_target_ctas")
+    return int(out.value)
+
+
+def _host_i32(x) -> torch.Tensor:
+    t = torch.as_tensor(x)
+    return t.detach().to("cpu", torch.int32).contiguous()
+
+
+@dataclass
+class Plan:
+    """A plan plus its chunk index arrays (host copies; device copies made on demand)."""
+
+    struct: PlanStruct
+    request_indices: torch.Tensor
+    kv_tile_indices: torch.Tensor
+    o_indptr: torch.Tensor
+    _dev: dict | None = None
+
+    def __getattr__(self, name):
+        if name.startswith("_") or name in ("struct",):
+            raise AttributeError(name)
+        return getattr(self.struct, name)
+
+    def device_arrays(self, device) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+        """(request_indices, kv_tile_indices, o_indptr) on `device`, uploaded once."""
+        key = str(torch.device(device))
+        if self._dev is None:
+            self._dev = {}
+        if key not in self._dev:
+            self._dev[key] = tuple(t.to(device) for t in (self.request_indices, self.kv_tile_indices, self.o_indptr))
+        return self._dev[key]
+
+
+def pa_v2_plan(indptr, last_page_len, first_page_offset, page_size: int, num_qo_heads: int, num_kv_heads: int,
+               head_dim: int, kv_dtype: int, target_ctas: int = 0, pages_per_chunk_override: int = 0,
+               seq_lens=None) -> Plan:
+    """Host plan (pa_v2_plan).  Inputs are host arrays (any int sequence / CPU tensor)."""
+    ip, lp, fp = _host_i32(indptr), _host_i32(last_page_len), _host_i32(first_page_offset)
+    batch = lp.numel()
+    sl = _host_i32(seq_lens) if seq_lens is not None else None
+    pages = (ip[1:] - ip[:-1]).clamp(min=1) if batch else ip[:0]
+    cap = int(pages.sum()) if batch else 0
+    ri = torch.zeros(max(cap, 1), dtype=torch.int32)
+    ti = torch.zeros(max(cap, 1), dtype=torch.int32)
+    oi = torch.zeros(batch + 1, dtype=torch.int32)
+    st = PlanStruct()
+    rc = lib().pa_v2_plan(ip.data_ptr(), lp.data_ptr(), fp.data_ptr(), sl.data_ptr() if sl is not None else None,
+                          batch, page_size, num_qo_heads, num_kv_heads, head_dim, kv_dtype, target_ctas,
+                          pages_per_chunk_override, ri.data_ptr(), ti.data_ptr(), cap, oi.data_ptr(),
+                          ctypes.byref(st))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_plan")
+    n = st.num_chunks
+    return Plan(st, ri[:n].clone(), ti[:n].clone(), oi)
+
+
+def pa_v2_plan_matches(plan: Plan, indptr, last_page_len, first_page_offset) -> bool:
+    ip, lp, fp = _host_i32(indptr), _host_i32(last_page_len), _host_i32(first_page_offset)
+    return bool(lib().pa_v2_plan_matches(ctypes.byref(plan.struct), ip.data_ptr(), lp.data_ptr(), fp.data_ptr(),
+                                         lp.numel()))
+
+
+def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pa_v2_decode_partial(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
+                         sm_scale: float, v_out=None, lse2_out=None, status=None, stream=None,
+                         request_indices=None, kv_tile_indices=None):
+    """Partial kernel (pa_v2_decode_partial).  Device tensors; returns (v_out [N,Hq,D], lse2_out [N,Hq])."""
+    s = plan.struct
+    dev = q.device
+    if request_indices is None or kv_tile_indices is None:
+        request_indices, kv_tile_indices, _ = plan.device_arrays(dev)
+    if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
+    if k_pool.dim() != 4 or tuple(k_pool.shape[1:]) != (s.page_size, s.num_kv_heads, s.head_dim):
+        raise ValueError(f"pools must be [P, {s.page_size}, {s.num_kv_heads}, {s.head_dim}]")
+    if v_out is None:
+        v_out = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    rc = lib().pa_v2_decode_partial(
+        ctypes.byref(s), _dev_ptr(q, "q", torch.float32), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+        KV_DTYPES[k_pool.dtype], k_pool.shape[0], _dev_ptr(indices, "indices", torch.int32), indices.numel(),
+        _dev_ptr(indptr, "indptr", torch.int32), _dev_ptr(last_page_len, "last_page_len", torch.int32),
+        _dev_ptr(first_page_offset, "first_page_offset", torch.int32),
+        _dev_ptr(request_indices, "request_indices", torch.int32),
+        _dev_ptr(kv_tile_indices, "kv_tile_indices", torch.int32), float(sm_scale),
+        _dev_ptr(v_out, "v_out", torch.float32), _dev_ptr(lse2_out, "lse2_out", torch.float32),
+        _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_decode_partial")
+    return v_out, lse2_out
+
+
+def pa_merge_states(v_in, lse2_in, o_indptr, num_rows_out: int, v_out=None, lse2_out=None, status=None,
+                    stream=None):
+    """Merge kernel (pa_merge_states).  Device tensors; returns (v_out [M,H,D], lse2_out [M,H])."""
+    N, H, D = v_in.shape
+    dev = v_in.device
+    if v_out is None:
+        v_out = torch.empty(num_rows_out, H, D, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(num_rows_out, H, device=dev, dtype=torch.float32)
+    rc = lib().pa_merge_states(_dev_ptr(v_in, "v_in", torch.float32), _dev_ptr(lse2_in, "lse2_in", torch.float32),
+                               _dev_ptr(o_indptr, "o_indptr", torch.int32), num_rows_out, N, H, D,
+                               _dev_ptr(v_out, "v_out", torch.float32),
+                               _dev_ptr(lse2_out, "lse2_out", torch.float32),
+                               _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_merge_states")
+    return v_out, lse2_out
+
+
+def decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, sm_scale: float,
+           out=None, lse2=None, workspace=None, status=None, stream=None):
+    """One decode step: the partial launch, then the merge launch when the plan needs one.
+
+    Returns (out [B, Hq, D] f32, lse2 [B, Hq] f32).  `workspace` may supply the
+    (v, lse) partial buffers sized by the plan.
+    """
+    s = plan.struct
+    ri, ti, oi = plan.device_arrays(q.device)
+    if not s.needs_merge:
+        v, l = pa_v2_decode_partial(plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
+                                    sm_scale, out, lse2, status, stream, ri, ti)
+        return v[:s.batch], l[:s.batch]
+    wv, wl = workspace if workspace is not None else (None, None)
+    wv, wl = pa_v2_decode_partial(plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
+                                  sm_scale, wv, wl, status, stream, ri, ti)
+    return pa_merge_states(wv, wl, oi, s.batch, out, lse2, status, stream)

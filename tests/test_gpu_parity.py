@@ -1,0 +1,228 @@
+"""GPU parity: the C-ABI CUDA path against the f64 oracle, element by element.
+
+Covers the five workloads at full size (in the launch configuration bench.py
+times: plan target from the device's SM count and occupancy), a sweep over head
+dims, GQA ratios, dtypes and page sizes with ragged lengths, mid-page window
+starts and empty requests, chunk-size invariance, the merge kernel alone, and
+the cascade composition.
+"""
+import math
+import random
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_attention_decode_gb300 import pa_v2 as pa
+from paged_attention_decode_gb300 import workloads as W
+from parity_helpers import LSE_TOL, OUT_TOL, assert_close, check_batch, make_plan, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    pa.lib()
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_csr_fixed_chunks():
+    b = W.tiny_csr()
+    plan, *_ = check_batch(b, target=1)
+    assert plan.num_chunks == 4 and plan.needs_merge == 1
+    assert plan.request_indices.tolist() == [0, 0, 1, 1] and plan.kv_tile_indices.tolist() == [0, 1, 0, 1]
+
+
+@pytest.fixture(scope="module")
+def llama():
+    return W.llama3_8b_32k()
+
+
+def test_llama3_8b_32k_bench_launch(llama):
+    plan, *_ = check_batch(llama)          # device-derived target: the launch bench.py times
+    assert plan.needs_merge == 1
+
+
+@pytest.mark.parametrize("target", [640, 152, 10 ** 6])
+def test_llama3_8b_32k_other_targets(llama, target):
+    check_batch(llama, target=target, check_partials=(target == 152))
+
+
+def test_sliding_window_batch():
+    check_batch(W.sliding_window_batch())
+
+
+def test_sparse_token_exact_full():
+    b = W.sparse_token_exact()
+    check_batch(b)
+
+
+def test_cascade_flat_and_two_level():
+    cb = W.cascade_shared_prefix()
+    f = cb.flat
+    _, flat_o, flat_l, _ = check_batch(f, check_partials=False)
+    co, cl = cascade_gpu(cb)
+    ref_o, ref_l = oracle.attention(f.q, f.k_pool, f.v_pool, f.indices, f.indptr, f.last_page_len,
+                                    f.first_page_offset, f.scale)
+    assert_close(co, cl, ref_o, ref_l, "cascade")
+    # the two levels partition the flat launch's key range: equal up to f32 rounding
+    assert float((co - flat_o).abs().max()) <= 2 * OUT_TOL
+
+
+def cascade_gpu(cb):
+    """Level 0 over the shared pages with stacked heads, level 1 over the suffixes, one merge."""
+    f = cb.flat
+    M, Hq, D = f.q.shape
+    Hkv = f.num_kv_heads
+    G = Hq // Hkv
+    dev = "cuda"
+    kp, vp = f.k_pool.to(dev), f.v_pool.to(dev)
+    dt = pa.KV_DTYPES[f.dtype]
+    npre = len(cb.prefix_indices)
+    # level 0: one request, M*G query heads per KV head, h0 = kv*(M*G) + m*G + g
+    q0 = f.q.to(dev).reshape(M, Hkv, G, D).permute(1, 0, 2, 3).reshape(1, Hkv * M * G, D).contiguous()
+    ip0 = torch.tensor([0, npre], dtype=torch.int32)
+    lp0 = torch.tensor([f.page_size], dtype=torch.int32)
+    fp0 = torch.tensor([0], dtype=torch.int32)
+    tgt0 = pa.pa_v2_default_target_ctas(M * Hq, Hkv, D, f.page_size, dt)
+    p0 = pa.pa_v2_plan(ip0, lp0, fp0, f.page_size, M * Hq, Hkv, D, dt, tgt0)
+    o0, l0 = pa.decode(p0, q0, kp, vp, cb.prefix_indices.to(dev), ip0.to(dev), lp0.to(dev), fp0.to(dev), f.scale)
+    # level 1: each member's private suffix
+    fp1 = torch.zeros(M, dtype=torch.int32)
+    tgt1 = pa.pa_v2_default_target_ctas(Hq, Hkv, D, f.page_size, dt)
+    p1 = pa.pa_v2_plan(cb.suffix_indptr, cb.suffix_last_page_len, fp1, f.page_size, Hq, Hkv, D, dt, tgt1)
+    o1, l1 = pa.decode(p1, f.q.to(dev), kp, vp, cb.suffix_indices.to(dev), cb.suffix_indptr.to(dev),
+                       cb.suffix_last_page_len.to(dev), fp1.to(dev), f.scale)
+    # unstack level 0 and pair each member's two states
+    o0 = o0.reshape(Hkv, M, G, D).permute(1, 0, 2, 3).reshape(M, Hq, D)
+    l0 = l0.reshape(Hkv, M, G).permute(1, 0, 2).reshape(M, Hq)
+    v_in = torch.stack([o0, o1], dim=1).reshape(2 * M, Hq, D).contiguous()
+    lse_in = torch.stack([l0, l1], dim=1).reshape(2 * M, Hq).contiguous()
+    oi = torch.arange(0, 2 * M + 1, 2, dtype=torch.int32, device=dev)
+    out, lse = pa.pa_merge_states(v_in, lse_in, oi, M)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# sweeps
+# ---------------------------------------------------------------------------
+
+SWEEP = [(dt, D, G, ps) for dt in (torch.float32, torch.float16, torch.bfloat16) for D in (64, 128)
+         for G in (1, 2, 3, 4, 8, 16) for ps in (1, 4, 5, 8, 16, 32, 64)]
+
+
+@pytest.mark.parametrize("dt,D,G,ps", SWEEP)
+def test_sweep_ragged(dt, D, G, ps):
+    rnd = random.Random(zlib.crc32(repr((str(dt), D, G, ps)).encode()))
+    B = 4
+    lens = [rnd.randint(1, 700), 0, rnd.randint(1, 40), rnd.randint(300, 1500)]
+    fpos = [rnd.randrange(ps) if L else 0 for L in lens]
+    Hkv = 2
+    b = W.make_batch("sweep", lens, fpos, ps, num_qo_heads=Hkv * G, num_kv_heads=Hkv, head_dim=D, dtype=dt,
+                     seed=rnd.randint(0, 10 ** 6), order="reversed" if G % 2 else "shuffled")
+    check_batch(b, target=rnd.choice([1, 64, 700]), override=rnd.choice([0, 0, 1, 3]))
+
+
+def test_chunk_size_invariance_seven_sizes():
+    b = W.make_batch("inv", [4099, 77, 1, 2500], [5, 0, 0, 15], 16, 32, 8, 128, torch.float16, seed=5)
+    outs = []
+    for ppc in (1, 2, 3, 7, 16, 64, 1000):
+        plan, o, lo, _ = check_batch(b, target=1, override=ppc, check_partials=(ppc in (1, 7)))
+        outs.append(o)
+    for o in outs[1:]:
+        assert float((o - outs[0]).abs().max()) <= OUT_TOL
+
+
+def test_empty_request_does_not_poison_neighbours():
+    b = W.make_batch("empty", [300, 0, 0, 45], [0, 0, 0, 3], 16, 8, 2, 128, torch.bfloat16, seed=9)
+    plan, o, lo, _ = check_batch(b, target=1000, override=1)
+    assert torch.all(o[1:3] == 0) and torch.all(lo[1:3] == -math.inf)
+    assert torch.isfinite(o).all() and torch.isfinite(lo[0]).all() and torch.isfinite(lo[3]).all()
+
+
+def test_single_token_and_full_final_pages():
+    # seq_len 1, a window that is exactly one full page, exactly full final pages
+    b = W.make_batch("edge", [1, 16, 32, 17, 15], [0, 0, 0, 15, 1], 16, 4, 4, 64, torch.float16, seed=2)
+    check_batch(b, target=1, override=1)
+    check_batch(b, target=10 ** 6)
+
+
+def test_nan_outside_sequences_is_never_read():
+    """Pool entries outside every request are NaN: any stray read shows up in the output."""
+    g = torch.Generator().manual_seed(4)
+    lens, fpos = [70, 5, 33], [3, 0, 9]
+    dk = [torch.randn(L, 2, 64, generator=g) for L in lens]
+    dv = [torch.randn(L, 2, 64, generator=g) for L in lens]
+    for dt in (torch.float16, torch.float32):
+        for ps in (1, 4, 16, 32):
+            fp = [f % ps for f in fpos]
+            b = W.scatter_dense("nan", dk, dv, fp, ps, num_qo_heads=8, seed=ps, dtype=dt)
+            check_batch(b, target=1, override=1)
+            check_batch(b, target=10 ** 6)
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+def test_cuda_core_kernel_on_16bit_pools(dt):
+    """plan.kernel = 1 selects the CUDA-core kernel for 16-bit pools (groups of up to 8 heads)."""
+    b = W.make_batch("simt16", [700, 33, 2100], [3, 0, 9], 16, 16, 2, 128, dt, seed=12)
+    plan = make_plan(b, target=200)
+    plan.struct.kernel = 1
+    check_batch(b, plan=plan)
+
+
+def test_plan_reuse_across_steps():
+    """A plan stays valid while no request crosses a page boundary (PR #984, What changed 4)."""
+    b = W.make_batch("reuse", [100, 200], [0, 0], 16, 8, 2, 128, torch.float16, seed=3)
+    plan = make_plan(b, target=300)
+    b2 = W.make_batch("reuse", [101, 201], [0, 0], 16, 8, 2, 128, torch.float16, seed=3)
+    assert pa.pa_v2_plan_matches(plan, b2.indptr, b2.last_page_len, b2.first_page_offset)
+    check_batch(b2, plan=plan)
+
+
+# ---------------------------------------------------------------------------
+# the merge kernel on its own
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128, 6])
+def test_merge_states_alone(D):
+    rng = np.random.default_rng(D)
+    groups = [1, 3, 0, 5, 2, 1, 7]
+    oi = np.concatenate([[0], np.cumsum(groups)]).astype(np.int32)
+    N, H = int(oi[-1]), 3
+    v = rng.standard_normal((N, H, D)).astype(np.float32)
+    l = rng.uniform(-30, 30, (N, H)).astype(np.float32)
+    l[4, 1] = -np.inf          # a -inf member contributes nothing
+    v[4, 1] = 0
+    l[9:11, :] = -np.inf       # an all-empty group (rows 9, 10 form group 4)
+    v[9:11] = 0
+    dev = "cuda"
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = pa.pa_merge_states(torch.from_numpy(v).to(dev), torch.from_numpy(l).to(dev),
+                                  torch.from_numpy(oi).to(dev), len(groups), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_o, ref_l = oracle.merge(v.astype(np.float64), l.astype(np.float64), oi)
+    assert_close(out, lse, ref_o, ref_l, "merge")
+    # a one-row group is an exact identity
+    assert torch.equal(out[0].cpu(), torch.from_numpy(v[0]))
+    assert torch.equal(lse[0].cpu(), torch.from_numpy(l[0]))
+
+
+def test_merge_regrouping_is_associative_on_gpu():
+    rng = np.random.default_rng(1)
+    N, H, D = 12, 4, 128
+    v = torch.from_numpy(rng.standard_normal((N, H, D)).astype(np.float32)).cuda()
+    l = torch.from_numpy(rng.uniform(-10, 10, (N, H)).astype(np.float32)).cuda()
+    full, fl = pa.pa_merge_states(v, l, torch.tensor([0, N], dtype=torch.int32, device="cuda"), 1)
+    part, pl = pa.pa_merge_states(v, l, torch.tensor([0, 5, 6, N], dtype=torch.int32, device="cuda"), 3)
+    again, al = pa.pa_merge_states(part, pl, torch.tensor([0, 3], dtype=torch.int32, device="cuda"), 1)
+    torch.cuda.synchronize()
+    assert float((again - full).abs().max()) <= 1e-5 and float((al - fl).abs().max()) <= 1e-5
