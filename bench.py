@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=32768)
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="time pa_v2_decode_partial + pa_merge_states instead of the one-launch pa_v2_decode")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
     ap.add_argument("--profile", type=int, default=0,
                     help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
@@ -278,18 +280,22 @@ def run_ours(args):
     partial_bytes = (kv_bytes + b0.q.numel() * 4 + b0.indices.numel() * 4 + N * 8
                      + N * Hq * (D + 1) * 4)
 
-    def step(i, ev=None):
+    counters = plan.device_counters(dev)
+
+    def step_two_launch(i):
         d = sets[i % len(sets)]
-        if ev is not None:
-            ev[0].record(stream)
         pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
                                 d.first_page_offset, b0.scale, wv, wl, None, stream, ri, ti)
-        if ev is not None:
-            ev[1].record(stream)
         if plan.needs_merge:
             pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
 
-    launches_per_step = 1 + int(plan.needs_merge)
+    def step_fused(i):
+        d = sets[i % len(sets)]
+        pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len, d.first_page_offset,
+                        b0.scale, out, lse, (wv, wl), counters, None, stream, ri, ti, oi)
+
+    step = step_two_launch if args.two_launch else step_fused
+    launches_per_step = 1 + int(plan.needs_merge) if args.two_launch else 1
 
     if args.profile:
         with torch.cuda.stream(stream):
@@ -306,7 +312,7 @@ def run_ours(args):
     stream.synchronize()
     import oracle
     ref_o, ref_l = oracle.attention(*oracle_sample(b0, args.context))
-    o_now = (out if plan.needs_merge else wv[:B]).cpu().double().numpy()
+    o_now = (out if (plan.needs_merge or not args.two_launch) else wv[:B]).cpu().double().numpy()
     err = float(abs(o_now - ref_o).max())
     if err > 2e-3:
         raise SystemExit(f"bench: GPU output disagrees with the oracle (max|d| = {err:.3e}); refusing to time")
@@ -364,16 +370,30 @@ def run_ours(args):
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
 
-    # per-launch duration of the dominant (partial) kernel: event pairs on its stream,
-    # eager launches over the same rotating inputs
-    n_ev = 300
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    # per-launch duration of the dominant (partial) kernel: a second timed region replaying a graph of
+    # partial launches only (same rotating inputs), CUDA events on the stream the kernel runs on
+    def partial_only(i):
+        d = sets[i % len(sets)]
+        pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                d.first_page_offset, b0.scale, wv, wl, None, stream, ri, ti)
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pgraph, stream=stream):
+        for i in range(G):
+            partial_only(i)
+    reps = max(1, min(args.steps, 20000) // G)
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(50_000_000)   # keep the GPU busy while the host enqueues every launch
-        for i in range(n_ev):
-            step(i, evs[i])
+        for _ in range(3):
+            pgraph.replay()
     stream.synchronize()
-    partial_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    p_start = torch.cuda.Event(enable_timing=True)
+    p_end = torch.cuda.Event(enable_timing=True)
+    p_start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            pgraph.replay()
+    p_end.record(stream)
+    stream.synchronize()
+    partial_ms = p_start.elapsed_time(p_end) / (reps * G)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
@@ -400,6 +420,7 @@ def run_ours(args):
                      "kernel": "pa_v2_partial_simt_kernel" if args.kernel == 1 else "pa_v2_partial_tc_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": partial_bytes, "launch_us": partial_ms * 1e3,
+                     "rest_of_step_us": ms_step * 1e3 - partial_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
@@ -426,6 +447,7 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     out = torch.empty(B, Hq, D, device=dev)
     lse = torch.empty(B, Hq, device=dev)
     ri, ti, oi = plan.device_arrays(dev)
+    counters = plan.device_counters(dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in[0])
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
 
@@ -438,15 +460,10 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
             for src, dst in zip(hi, di):
                 dst.copy_(src, non_blocking=True)
             q, idx, ip, lp, fp = di
-            pa.pa_v2_decode_partial(plan, q, sets[k].k_pool, sets[k].v_pool, idx, ip, lp, fp, b0.scale, wv, wl,
-                                    None, stream, ri, ti)
-            if plan.needs_merge:
-                pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
-                out_h.copy_(out, non_blocking=True)
-                lse_h.copy_(lse, non_blocking=True)
-            else:
-                out_h.copy_(wv[:B], non_blocking=True)
-                lse_h.copy_(wl[:B], non_blocking=True)
+            pa.pa_v2_decode(plan, q, sets[k].k_pool, sets[k].v_pool, idx, ip, lp, fp, b0.scale, out, lse, (wv, wl),
+                            counters, None, stream, ri, ti, oi)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
         stream.synchronize()
 
     for i in range(20):
@@ -459,7 +476,7 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     kv_bytes = b0.kv_bytes()
     return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pa_v2_plan_matches + pa_v2_decode_partial + pa_merge_states via the ctypes binding"}
+            "path": "pa_v2_plan_matches + pa_v2_decode via the ctypes binding"}
 
 
 def main():

@@ -96,6 +96,7 @@ typedef struct pa_v2_plan_t {
     int64_t num_indices;              /* indptr[batch] */
     int64_t workspace_v_bytes;        /* num_chunks * num_qo_heads * head_dim * 4 */
     int64_t workspace_lse_bytes;      /* num_chunks * num_qo_heads * 4 */
+    int64_t counter_bytes;            /* batch * num_kv_heads * q_groups * 4 (pa_v2_decode) */
     uint64_t geometry_hash;           /* FNV-1a of batch and per-request page counts */
 } pa_v2_plan_t;
 
@@ -166,6 +167,31 @@ pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const v
                                const int32_t* request_indices, const int32_t* kv_tile_indices,
                                float sm_scale, float* v_out, float* lse2_out, int32_t* status,
                                void* cuda_stream);
+
+/* One-launch decode step: the partial kernel above with the merge of
+ * pa_merge_states fused into it (the "write O directly" single-chunk case and
+ * the multi-chunk merge of issue #898, Task 2-3, in one kernel).  Every CTA
+ * writes its chunk's partial to the workspace and takes a ticket on the
+ * counter of its (request, kv head, q-head group); the CTA holding the last
+ * ticket merges all chunks of that request for its heads (closed form of
+ * design piece 3) into out / lse2_out and sets the counter back to 0.  No CTA
+ * ever waits for another.  A request with one chunk is written straight to
+ * out.  Results equal pa_v2_decode_partial + pa_merge_states up to f32
+ * rounding order.
+ *   o_indptr      [batch + 1] device, the plan's o_indptr
+ *   workspace_v / workspace_lse: as v_out / lse2_out of pa_v2_decode_partial
+ *   counters      [plan->counter_bytes / 4] device int32, ALL ZERO before the
+ *                 first call; the kernel leaves them zero.  After a call that
+ *                 failed on the device (status word non-zero), zero them again.
+ *   out [batch, num_qo_heads, head_dim] f32, lse2_out [batch, num_qo_heads] f32.
+ * Other arguments, layouts and errors as pa_v2_decode_partial.  Two calls
+ * sharing `counters` must not overlap on the GPU. */
+pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
+                       int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
+                       const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
+                       const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                       float sm_scale, float* workspace_v, float* workspace_lse, int32_t* counters, float* out,
+                       float* lse2_out, int32_t* status, void* cuda_stream);
 
 /* The variable-length merge (issue #898, design piece 3 and Task 3; PR
  * #984, What changed 3).  For output row r and head h, the rows

@@ -26,9 +26,16 @@ struct PartialParams {
   const int32_t* kv_tile_indices;
   const void* k_pool;   // used by the cp.async staging path
   const void* v_pool;
-  float* v_out;
-  float* lse_out;
+  float* v_out;        // partial workspace [num_chunks, Hq, D]
+  float* lse_out;      // partial workspace [num_chunks, Hq]
   int32_t* status;
+  // fused decode (pa_v2_decode): the last CTA of a (request, kv head, q-group)
+  // merges that request's chunks into out / lse_final
+  const int32_t* o_indptr;
+  int32_t* counters;   // [batch * gridDim.y], zero between launches
+  float* out;          // [batch, Hq, D]
+  float* lse_final;    // [batch, Hq]
+  int32_t fused;
   int64_t num_pages;
   int64_t num_indices;
   int32_t batch;
@@ -70,6 +77,7 @@ struct ChunkGeom {
   int32_t s_end;       // one past the last slot
   int32_t fpo, lpl;
   int32_t n_stages;
+  bool bad;            // request or page-slot range out of bounds (recorded in the status word)
 };
 
 struct StageGeom {
@@ -111,6 +119,7 @@ __device__ __forceinline__ ChunkGeom chunk_geom(const PartialParams& p, int c, i
   } else {
     g.n_stages = (g.s_end - g.s_begin) * (ps / kStageRows);
   }
+  g.bad = bad;
   *r_out = r;
   return g;
 }
@@ -137,24 +146,25 @@ __device__ __forceinline__ StageGeom stage_geom(const ChunkGeom& g, int j, int p
   return s;
 }
 
-// Merge the per-warp online-softmax states of a CTA and write the chunk's
-// normalized output and lse2.  ms/ls: [kWarps][HP]; accs: [kWarps][HP][D]
-// (unnormalized, relative to each warp's max).  Called by all threads after a
-// __syncthreads() that follows the state writes.
-template <int HP, int D>
+// Merge the per-warp online-softmax states of a CTA of NW warps and write the
+// chunk's normalized output and lse2 to row `row` of (v_dst, lse_dst).  ms/ls:
+// [NW][HP]; accs: [NW][HP][D] (unnormalized, relative to each warp's max).
+// Called by all threads after a __syncthreads() that follows the state writes.
+template <int HP, int D, int NW>
 __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, const float* ms, const float* ls,
-                                                        const float* accs, int c, int h_first, int nheads) {
-  for (int idx = threadIdx.x; idx < nheads * D; idx += kWarps * 32) {
+                                                        const float* accs, size_t row, int h_first, int nheads,
+                                                        float* v_dst, float* lse_dst) {
+  for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
     const int h = idx / D;
     const int d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms[w * HP + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * HP + h]);
     float out = 0.f, lse = -INFINITY;
     if (M != -INFINITY) {
       float L = 0.f, A = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float wgt = fast_exp2(ms[w * HP + h] - M);
         L += ls[w * HP + h] * wgt;
         A += accs[(w * HP + h) * D + d] * wgt;
@@ -162,9 +172,161 @@ __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, 
       out = A / L;
       lse = M + fast_log2(L);
     }
-    const size_t row = (size_t)c * p.num_qo_heads + h_first + h;
-    p.v_out[row * D + d] = out;
-    if (d == 0) p.lse_out[row] = lse;
+    const size_t o = row * p.num_qo_heads + h_first + h;
+    v_dst[o * D + d] = out;
+    if (d == 0) lse_dst[o] = lse;
+  }
+}
+
+// Fused merge (pa_v2_decode).  After a CTA has written its chunk's partial to
+// the workspace, thread 0 takes a ticket on the counter of its (request, kv
+// head, q-group) with an acq_rel atomic; the __syncthreads() before it makes
+// the whole CTA's writes part of that release.  The CTA that takes the last
+// ticket merges every chunk of the request for its heads with the closed form
+// of issue #898, design piece 3 (m = max lse_i, w_i = 2^(lse_i - m),
+// v = sum w_i v_i / sum w_i, lse = log2(sum w_i) + m) and resets the counter.
+// No CTA waits on another: the first n-1 arrivals just leave.
+//
+// The merge is bound by L2 latency, so each thread issues all the loads of a
+// batch at once: it owns one (head, 4-float slice) and a 1/split share of the
+// chunks, reads up to 16 chunks' LSE and slice in one round, and folds them
+// into a running (max, weight sum, accumulator) -- the same closed form applied
+// batch by batch.  The shares of a slice then meet in shared memory.
+// scratch: >= 6 * NW * 32 floats of shared memory no longer in use.
+template <int D, int NW>
+__device__ __forceinline__ void fused_merge(const PartialParams& p, float* scratch, int r, int h_first,
+                                            int nheads, int num_chunks) {
+  __shared__ int s_last;
+  constexpr int NT = NW * 32;
+  constexpr int Q = D / 4;   // float4 slices per head row
+  constexpr int B = 16;      // chunks per round of loads
+  const int n0 = p.o_indptr[r];
+  const int n1 = p.o_indptr[r + 1];
+  if (n0 < 0 || n1 < n0 || n1 > num_chunks) {
+    if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_INDPTR);
+    return;
+  }
+  __syncthreads();  // every thread's partial stores precede the release below
+  if (threadIdx.x == 0) {
+    int* ctr = p.counters + (size_t)r * gridDim.y + blockIdx.y;
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+    const int last = prev == (n1 - n0) - 1;
+    if (last) atomicExch(ctr, 0);  // every arrival is in: ready for the next launch
+    s_last = last;
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  const int tid = threadIdx.x;
+  const size_t hq = (size_t)p.num_qo_heads;
+  const int units = nheads * Q;
+  const int split = units >= NT ? 1 : NT / units;  // threads sharing one slice (chunk-parallel)
+  const int sub = tid / units;
+  float* sm_m = scratch;                                     // [NT]
+  float* sm_w = scratch + NT;                                // [NT]
+  float4* sm_a = reinterpret_cast<float4*>(scratch + 2 * NT);  // [NT]
+
+  for (int ub = 0; ub < units; ub += NT) {
+    const int u = ub + (tid % units);
+    const bool working = sub < split && u < units;
+    const int head = h_first + u / Q;
+    const int quad = u % Q;
+    float m = -INFINITY, W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (working) {
+      for (int c = n0 + sub; c < n1; c += B * split) {
+        float l[B];
+        float4 v[B];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+          const int cc = c + k * split;
+          const bool ok = cc < n1;
+          l[k] = ok ? __ldcg(p.lse_out + cc * hq + head) : -INFINITY;
+          v[k] = ok ? __ldcg(reinterpret_cast<const float4*>(p.v_out + (cc * hq + head) * D) + quad)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < B; ++k) mb = fmaxf(mb, l[k]);
+        if (mb == -INFINITY) continue;
+        const float sc = fast_exp2(m - mb);  // m = -inf -> 0
+        W *= sc;
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+          const float w = l[k] == -INFINITY ? 0.f : fast_exp2(l[k] - mb);
+          W += w;
+          acc.x = fmaf(w, v[k].x, acc.x);
+          acc.y = fmaf(w, v[k].y, acc.y);
+          acc.z = fmaf(w, v[k].z, acc.z);
+          acc.w = fmaf(w, v[k].w, acc.w);
+        }
+        m = mb;
+      }
+    }
+    if (split > 1) {
+      sm_m[tid] = m;
+      sm_w[tid] = W;
+      sm_a[tid] = acc;
+      __syncthreads();
+      if (working && sub == 0) {
+        float M = m;
+        for (int s = 1; s < split; ++s) M = fmaxf(M, sm_m[tid + s * units]);
+        float Wt = 0.f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+          for (int s = 0; s < split; ++s) {
+            const int t2 = tid + s * units;
+            const float sc = sm_m[t2] == -INFINITY ? 0.f : fast_exp2(sm_m[t2] - M);
+            Wt += sm_w[t2] * sc;
+            A.x += sm_a[t2].x * sc;
+            A.y += sm_a[t2].y * sc;
+            A.z += sm_a[t2].z * sc;
+            A.w += sm_a[t2].w * sc;
+          }
+        }
+        m = M;
+        W = Wt;
+        acc = A;
+      }
+    }
+    if (working && sub == 0) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lse = -INFINITY;
+      if (m != -INFINITY && W > 0.f) {
+        o = make_float4(acc.x / W, acc.y / W, acc.z / W, acc.w / W);
+        lse = m + fast_log2(W);
+      }
+      reinterpret_cast<float4*>(p.out + ((size_t)r * hq + head) * D)[quad] = o;
+      if (quad == 0) p.lse_final[(size_t)r * hq + head] = lse;
+    }
+  }
+}
+
+// The end of every partial kernel: write the chunk's state, then (fused
+// decode) merge the request when this CTA is the last of its group.  A request
+// with a single chunk writes straight to the final output.  scratch: the CTA's
+// shared memory that is free once the states have been combined.
+template <int HP, int D, int NW>
+__device__ __forceinline__ void finish_chunk(const PartialParams& p, const ChunkGeom& g, const float* ms,
+                                             const float* ls, const float* accs, float* scratch, int c, int r,
+                                             int h_first, int nheads) {
+  bool direct = false;
+  if (p.fused && !g.bad) {
+    const int n0 = p.o_indptr[r], n1 = p.o_indptr[r + 1];
+    direct = n1 - n0 == 1;
+  }
+  if (direct)
+    combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, (size_t)r, h_first, nheads, p.out, p.lse_final);
+  else
+    combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, (size_t)c, h_first, nheads, p.v_out, p.lse_out);
+  if (p.fused && !g.bad && !direct) {
+    __syncthreads();  // scratch aliases the state arrays just read
+    fused_merge<D, NW>(p, scratch, r, h_first, nheads, gridDim.x);
   }
 }
 

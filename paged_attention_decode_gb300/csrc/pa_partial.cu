@@ -119,22 +119,31 @@ extern "C" pa_status pa_v2_default_target_ctas(int32_t device, int32_t num_qo_he
   return PA_OK;
 }
 
-extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
-                                          const void* v_pool, int32_t kv_dtype, int64_t num_pages,
-                                          const int32_t* indices, int64_t num_indices, const int32_t* indptr,
-                                          const int32_t* last_page_len, const int32_t* first_page_offset,
-                                          const int32_t* request_indices, const int32_t* kv_tile_indices,
-                                          float sm_scale, float* v_out, float* lse2_out, int32_t* status,
-                                          void* cuda_stream) {
+namespace {
+
+struct FusedArgs {
+  const int32_t* o_indptr;
+  int32_t* counters;
+  float* out;
+  float* lse_final;
+};
+
+pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
+                        int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
+                        const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
+                        const int32_t* request_indices, const int32_t* kv_tile_indices, float sm_scale,
+                        float* v_out, float* lse2_out, int32_t* status, void* cuda_stream, const FusedArgs* fused) {
   if (!plan) return PA_EINVAL;
   if (plan->num_chunks == 0) return PA_OK;
   if (!q || !k_pool || !v_pool || !indices || !indptr || !last_page_len || !first_page_offset ||
       !request_indices || !kv_tile_indices || !v_out || !lse2_out)
     return PA_EINVAL;
+  if (fused && (!fused->o_indptr || !fused->counters || !fused->out || !fused->lse_final)) return PA_EINVAL;
   if (kv_dtype != plan->kv_dtype || num_pages < 1 || num_indices < plan->num_indices || plan->num_chunks < 0 ||
       plan->num_kv_heads < 1 || plan->q_groups < 1 || plan->page_size < 1 || !std::isfinite(sm_scale))
     return PA_EINVAL;
-  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) || !pa::aligned16(v_out))
+  if (!pa::aligned16(q) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) || !pa::aligned16(v_out) ||
+      (fused && !pa::aligned16(fused->out)))
     return PA_EINVAL;
   const int D = plan->head_dim;
   const int ps = plan->page_size;
@@ -159,6 +168,7 @@ extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float*
 
   pa::LaunchArgs a;
   pa::PartialParams& p = a.p;
+  std::memset(&p, 0, sizeof(p));
   p.q = q;
   p.indices = indices;
   p.indptr = indptr;
@@ -171,6 +181,13 @@ extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float*
   p.v_out = v_out;
   p.lse_out = lse2_out;
   p.status = status;
+  if (fused) {
+    p.o_indptr = fused->o_indptr;
+    p.counters = fused->counters;
+    p.out = fused->out;
+    p.lse_final = fused->lse_final;
+    p.fused = 1;
+  }
   p.num_pages = num_pages;
   p.num_indices = num_indices;
   p.batch = plan->batch;
@@ -192,4 +209,31 @@ extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float*
   a.num_chunks = plan->num_chunks;
   a.stream = static_cast<cudaStream_t>(cuda_stream);
   return (pa_status)(tc ? pa::launch_partial_tc(a, tma) : pa::launch_partial_simt(a));
+}
+
+}  // namespace
+
+extern "C" pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
+                                          const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                          const int32_t* indices, int64_t num_indices, const int32_t* indptr,
+                                          const int32_t* last_page_len, const int32_t* first_page_offset,
+                                          const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                          float sm_scale, float* v_out, float* lse2_out, int32_t* status,
+                                          void* cuda_stream) {
+  return launch_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr, last_page_len,
+                       first_page_offset, request_indices, kv_tile_indices, sm_scale, v_out, lse2_out, status,
+                       cuda_stream, nullptr);
+}
+
+extern "C" pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
+                                  int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
+                                  const int32_t* indptr, const int32_t* last_page_len,
+                                  const int32_t* first_page_offset, const int32_t* request_indices,
+                                  const int32_t* kv_tile_indices, const int32_t* o_indptr, float sm_scale,
+                                  float* workspace_v, float* workspace_lse, int32_t* counters, float* out,
+                                  float* lse2_out, int32_t* status, void* cuda_stream) {
+  const FusedArgs f{o_indptr, counters, out, lse2_out};
+  return launch_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr, last_page_len,
+                       first_page_offset, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse,
+                       status, cuda_stream, &f);
 }

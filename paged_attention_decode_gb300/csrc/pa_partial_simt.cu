@@ -187,6 +187,14 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   };
 
+  // ---- prologue: fill the ring ----
+#pragma unroll
+  for (int s = 0; s < NSW; ++s) {
+    const int j = warp + s * kWarps;
+    if (j < g.n_stages) issue(j, s, stage_page(j));
+  }
+  int32_t next_page = stage_page(warp + NSW * kWarps);
+
   // ---- queries of the group, pre-scaled into base 2 ----
   float qf[HP][VEC];
 #pragma unroll
@@ -207,13 +215,6 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
 
-  // ---- prologue: fill the ring ----
-#pragma unroll
-  for (int s = 0; s < NSW; ++s) {
-    const int j = warp + s * kWarps;
-    if (j < g.n_stages) issue(j, s, stage_page(j));
-  }
-  int32_t next_page = stage_page(warp + NSW * kWarps);
 
   float acc[HP][VEC];
 #pragma unroll
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
   __syncthreads();
-  combine_warps_and_store<HP, D>(p, ms, ls, accs, c, h_first, nheads);
+  finish_chunk<HP, D, kWarps>(p, g, ms, ls, accs, accs, c, r, h_first, nheads);
 }
 
 // ---- host side --------------------------------------------------------------

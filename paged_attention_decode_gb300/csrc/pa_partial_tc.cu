@@ -119,28 +119,29 @@ __device__ __forceinline__ uint32_t swz(int row, int ch) {
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int D, int NT, int NSW>
+template <int D, int NT, int NSW, int NW>
 struct TcLayout {
   static constexpr int HP = 8 * NT;                 // query heads per CTA (padded)
   static constexpr int TILE = (D / 64) * 2048;       // bytes of one side of a stage
   static constexpr int STAGE = 2 * TILE;
-  static constexpr int STAGES_BYTES = kWarps * NSW * STAGE;
-  static constexpr int PT_BYTES = kWarps * 2 * HP * 32;   // P^T hi/lo per warp: [HP][16] 16-bit
-  static constexpr int STATE_BYTES = kWarps * HP * D * 4;
+  static constexpr int STAGES_BYTES = NW * NSW * STAGE;
+  static constexpr int PT_BYTES = NW * 2 * HP * 32;   // P^T hi/lo per warp: [HP][16] 16-bit
+  static constexpr int STATE_BYTES = NW * HP * D * 4;
   static constexpr int BODY = STAGES_BYTES > STATE_BYTES ? STAGES_BYTES : STATE_BYTES;
   static constexpr int BARS = BODY + PT_BYTES;
-  static constexpr int MS = BARS + kWarps * NSW * 8;
-  static constexpr int TOTAL = MS + 2 * kWarps * HP * 4;
+  static constexpr int MS = BARS + NW * NSW * 8;
+  static constexpr int TOTAL = MS + 2 * NW * HP * 4;
   static constexpr int ALLOC = TOTAL + 1024;         // room to align the base to 1 KB
 };
 
 // T: __half or __nv_bfloat16.  D: 64 or 128.  NT: 8-head n-tiles per CTA (1 or
-// 2).  NSW: stage ring depth per warp.  USE_TMA: staging mechanism.
-template <typename T, int D, int NT, int NSW, bool USE_TMA>
-__global__ void __launch_bounds__(kWarps * 32)
+// 2).  NSW: stage ring depth per warp.  NW: warps per CTA.  USE_TMA: staging
+// mechanism.
+template <typename T, int D, int NT, int NSW, int NW, bool USE_TMA>
+__global__ void __launch_bounds__(NW * 32)
     pa_v2_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const PartialParams p) {
-  using L = TcLayout<D, NT, NSW>;
+  using L = TcLayout<D, NT, NSW, NW>;
   constexpr int HP = L::HP;
   constexpr int KSTEPS = D / 16;
   constexpr int CPR = D / 8;  // 16-byte chunks per K/V row
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BARS);
   float* ms = reinterpret_cast<float*>(smem + L::MS);
-  float* ls = ms + kWarps * HP;
+  float* ls = ms + NW * HP;
   float* accs = reinterpret_cast<float*>(smem);
 
   const int warp = threadIdx.x >> 5;
@@ -181,33 +182,6 @@ __global__ void __launch_bounds__(kWarps * 32)
       fence_barrier_init();
     }
     __syncwarp();
-  }
-
-  // ---- Q fragments: B operand of S^T = K Q^T, base-2 scaled, split hi + lo ----
-  uint32_t qh[KSTEPS][NT][2], ql[KSTEPS][NT][2];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int head = 8 * j + g;
-    const bool ok = head < nheads;
-    const float* qp = p.q + ((size_t)r * p.num_qo_heads + h_first + (ok ? head : 0)) * D + 2 * t;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      float x[4];
-      x[0] = ok ? qp[16 * kk] * p.scale_log2 : 0.f;
-      x[1] = ok ? qp[16 * kk + 1] * p.scale_log2 : 0.f;
-      x[2] = ok ? qp[16 * kk + 8] * p.scale_log2 : 0.f;
-      x[3] = ok ? qp[16 * kk + 9] * p.scale_log2 : 0.f;
-      float h[4], l[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        h[e] = TC<T>::round(x[e]);
-        l[e] = x[e] - h[e];
-      }
-      qh[kk][j][0] = TC<T>::pack(h[0], h[1]);
-      qh[kk][j][1] = TC<T>::pack(h[2], h[3]);
-      ql[kk][j][0] = TC<T>::pack(l[0], l[1]);
-      ql[kk][j][1] = TC<T>::pack(l[2], l[3]);
-    }
   }
 
   // ---- staging ----
@@ -277,11 +251,40 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 #pragma unroll
   for (int s = 0; s < NSW; ++s) {
-    const int j = warp + s * kWarps;
+    const int j = warp + s * NW;
     if (j < gm.n_stages) issue(j, s, stage_page(j));
     if (!USE_TMA) cp_async_commit();
   }
-  int32_t next_page = stage_page(warp + NSW * kWarps);
+  int32_t next_page = stage_page(warp + NSW * NW);
+
+  // ---- Q fragments (loaded while the first stages stream in): B operand of
+  // S^T = K Q^T, base-2 scaled, split hi + lo ----
+  uint32_t qh[KSTEPS][NT][2], ql[KSTEPS][NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int head = 8 * j + g;
+    const bool ok = head < nheads;
+    const float* qp = p.q + ((size_t)r * p.num_qo_heads + h_first + (ok ? head : 0)) * D + 2 * t;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      float x[4];
+      x[0] = ok ? qp[16 * kk] * p.scale_log2 : 0.f;
+      x[1] = ok ? qp[16 * kk + 1] * p.scale_log2 : 0.f;
+      x[2] = ok ? qp[16 * kk + 8] * p.scale_log2 : 0.f;
+      x[3] = ok ? qp[16 * kk + 9] * p.scale_log2 : 0.f;
+      float h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = TC<T>::round(x[e]);
+        l[e] = x[e] - h[e];
+      }
+      qh[kk][j][0] = TC<T>::pack(h[0], h[1]);
+      qh[kk][j][1] = TC<T>::pack(h[2], h[3]);
+      ql[kk][j][0] = TC<T>::pack(l[0], l[1]);
+      ql[kk][j][1] = TC<T>::pack(l[2], l[3]);
+    }
+  }
+
 
   float o[KSTEPS][NT][4];
 #pragma unroll
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   int i = 0;
   for (;; ++i) {
-    const int j = warp + i * kWarps;
+    const int j = warp + i * NW;
     if (j >= gm.n_stages) break;
     const int slot = i % NSW;
     if (USE_TMA) {
@@ -428,11 +431,11 @@ __global__ void __launch_bounds__(kWarps * 32)
     __syncwarp();
 
     // ---- refill this slot with the warp's stage NSW rounds ahead ----
-    const int jn = warp + (i + NSW) * kWarps;
+    const int jn = warp + (i + NSW) * NW;
     if (jn < gm.n_stages) {
       if (USE_TMA) fence_proxy_async_smem();
       issue(jn, slot, next_page);
-      next_page = stage_page(jn + kWarps);
+      next_page = stage_page(jn + NW);
     }
     if (!USE_TMA) cp_async_commit();
   }
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (failed) {
       if (lane == 0) report(p.status, PA_DEVICE_WAIT_TIMEOUT);
       for (int k = i + 1; k < i + NSW; ++k) {
-        if (warp + k * kWarps >= gm.n_stages) break;
+        if (warp + k * NW >= gm.n_stages) break;
         mbar_wait_bounded(&mybar[k % NSW], (k / NSW) & 1, kWaitLimitCycles);
       }
     }
@@ -480,13 +483,14 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
   __syncthreads();
-  combine_warps_and_store<HP, D>(p, ms, ls, accs, c, h_first, nheads);
+  finish_chunk<HP, D, NW>(p, gm, ms, ls, accs, accs, c, r, h_first, nheads);
 }
 
 // ---- host side --------------------------------------------------------------
 
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const PartialParams);
-constexpr int kTcRing = 3;
+constexpr int kTcRing = 3;   // stages in flight per warp
+constexpr int kTcWarps = 8;  // one CTA of 8 warps per SM: 8 x 3 x 8 KB of stages
 
 struct TcInstance {
   TcKernel fn;
@@ -495,7 +499,7 @@ struct TcInstance {
 
 template <typename T, int D, int NT, bool TMA>
 TcInstance tc_make() {
-  return {pa_v2_partial_tc_kernel<T, D, NT, kTcRing, TMA>, (size_t)TcLayout<D, NT, kTcRing>::ALLOC};
+  return {pa_v2_partial_tc_kernel<T, D, NT, kTcRing, kTcWarps, TMA>, (size_t)TcLayout<D, NT, kTcRing, kTcWarps>::ALLOC};
 }
 
 template <typename T, int D, bool TMA>
@@ -528,7 +532,7 @@ int launch_partial_tc(const LaunchArgs& a, bool use_tma) {
   if (!tc_pick(a.kv_dtype, a.head_dim, a.p.hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
   if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
   dim3 grid(a.num_chunks, a.p.num_kv_heads * a.p.q_groups);
-  inst.fn<<<grid, kWarps * 32, inst.smem, a.stream>>>(*a.tm_k, *a.tm_v, a.p);
+  inst.fn<<<grid, kTcWarps * 32, inst.smem, a.stream>>>(*a.tm_k, *a.tm_v, a.p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
@@ -536,7 +540,7 @@ int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int*
   TcInstance inst;
   if (!tc_pick(kv_dtype, head_dim, hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
   if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, inst.fn, kWarps * 32, inst.smem) ==
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, inst.fn, kTcWarps * 32, inst.smem) ==
                  cudaSuccess
              ? PA_OK
              : PA_ECUDA;

@@ -138,6 +138,7 @@ pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len, const 
   out->num_indices = nnz;
   out->workspace_v_bytes = n * num_qo_heads * static_cast<int64_t>(head_dim) * 4;
   out->workspace_lse_bytes = n * num_qo_heads * 4;
+  out->counter_bytes = static_cast<int64_t>(batch) * per_chunk * 4;
   out->geometry_hash = geometry_hash(indptr, batch);
   if (n > cap_chunks) return PA_ECAPACITY;
 

@@ -29,8 +29,8 @@ KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF
 
 # Exported symbols of the C ABI (the header's declarations).
 ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
-               "pa_v2_decode_partial", "pa_merge_states", "pa_status_from_device", "pa_status_string",
-               "pa_version")
+               "pa_v2_decode_partial", "pa_v2_decode", "pa_merge_states", "pa_status_from_device",
+               "pa_status_string", "pa_version")
 
 
 class PaError(RuntimeError):
@@ -47,7 +47,8 @@ class PlanStruct(ctypes.Structure):
         "q_groups", "pages_per_chunk", "lo_pages_per_chunk", "hi_pages_per_chunk", "num_chunks",
         "needs_merge", "target_ctas", "total_ctas", "kernel")] + [
         ("num_indices", ctypes.c_int64), ("workspace_v_bytes", ctypes.c_int64),
-        ("workspace_lse_bytes", ctypes.c_int64), ("geometry_hash", ctypes.c_uint64)]
+        ("workspace_lse_bytes", ctypes.c_int64), ("counter_bytes", ctypes.c_int64),
+        ("geometry_hash", ctypes.c_uint64)]
 
 
 _lib = None
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_plan_matches.restype = i32
         L.pa_v2_decode_partial.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, f32, P, P, P, P]
         L.pa_v2_decode_partial.restype = i32
+        L.pa_v2_decode.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P, P, P, P]
+        L.pa_v2_decode.restype = i32
         L.pa_merge_states.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
         L.pa_merge_states.restype = i32
         L.pa_status_from_device.argtypes = [i32]
@@ -129,6 +132,16 @@ class Plan:
         if name.startswith("_") or name in ("struct",):
             raise AttributeError(name)
         return getattr(self.struct, name)
+
+    def device_counters(self, device) -> torch.Tensor:
+        """Zeroed int32 ticket counters for pa_v2_decode on `device`, allocated once (the kernel leaves
+        them zero after every successful launch)."""
+        key = "counters:" + str(torch.device(device))
+        if self._dev is None:
+            self._dev = {}
+        if key not in self._dev:
+            self._dev[key] = torch.zeros(max(1, self.struct.counter_bytes // 4), dtype=torch.int32, device=device)
+        return self._dev[key]
 
     def device_arrays(self, device) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
         """(request_indices, kv_tile_indices, o_indptr) on `device`, uploaded once."""
@@ -234,6 +247,50 @@ def pa_merge_states(v_in, lse2_in, o_indptr, num_rows_out: int, v_out=None, lse2
     if rc != PA_OK:
         raise PaError(rc, "pa_merge_states")
     return v_out, lse2_out
+
+
+def pa_v2_decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
+                 sm_scale: float, out=None, lse2_out=None, workspace=None, counters=None, status=None, stream=None,
+                 request_indices=None, kv_tile_indices=None, o_indptr=None):
+    """One-launch decode (pa_v2_decode): partial kernel with the merge fused in.
+
+    Returns (out [B, Hq, D] f32, lse2 [B, Hq] f32).  `workspace` = (v, lse) partial buffers sized by the
+    plan; `counters` = zeroed int32 [plan.counter_bytes // 4] (the plan keeps one per device by default).
+    """
+    s = plan.struct
+    dev = q.device
+    ri, ti, oi = plan.device_arrays(dev)
+    ri = ri if request_indices is None else request_indices
+    ti = ti if kv_tile_indices is None else kv_tile_indices
+    oi = oi if o_indptr is None else o_indptr
+    if counters is None:
+        counters = plan.device_counters(dev)
+    wv, wl = workspace if workspace is not None else (None, None)
+    if wv is None:
+        wv = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+    if wl is None:
+        wl = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    if out is None:
+        out = torch.empty(max(s.batch, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(max(s.batch, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
+    if counters.numel() * 4 < s.counter_bytes:
+        raise ValueError("counters too small for the plan")
+    rc = lib().pa_v2_decode(
+        ctypes.byref(s), _dev_ptr(q, "q", torch.float32), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+        KV_DTYPES[k_pool.dtype], k_pool.shape[0], _dev_ptr(indices, "indices", torch.int32), indices.numel(),
+        _dev_ptr(indptr, "indptr", torch.int32), _dev_ptr(last_page_len, "last_page_len", torch.int32),
+        _dev_ptr(first_page_offset, "first_page_offset", torch.int32),
+        _dev_ptr(ri, "request_indices", torch.int32), _dev_ptr(ti, "kv_tile_indices", torch.int32),
+        _dev_ptr(oi, "o_indptr", torch.int32), float(sm_scale), _dev_ptr(wv, "workspace_v", torch.float32),
+        _dev_ptr(wl, "workspace_lse", torch.float32), _dev_ptr(counters, "counters", torch.int32),
+        _dev_ptr(out, "out", torch.float32), _dev_ptr(lse2_out, "lse2_out", torch.float32),
+        _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_decode")
+    return out[:s.batch], lse2_out[:s.batch]
 
 
 def decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, sm_scale: float,

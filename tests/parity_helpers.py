@@ -54,13 +54,35 @@ def run_gpu(b, plan, d=None):
     return v[:plan.num_chunks], l[:plan.num_chunks], o, lo, int(status.item())
 
 
-def check_batch(b, plan=None, target=None, override=None, check_partials=True, d=None):
+def run_gpu_fused(b, plan, d=None):
+    """The one-launch decode (pa_v2_decode), twice in a row on the same counters.  Returns (out, lse, status)."""
+    d = d if d is not None else b.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(2):
+        o, lo = pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                d.first_page_offset, b.scale, status=status)
+        outs.append((o.clone(), lo.clone()))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]), \
+        "fused decode is not repeatable (ticket counters not reset?)"
+    if plan.num_chunks:
+        assert int(plan.device_counters("cuda").abs().sum()) == 0, "ticket counters left non-zero"
+    return outs[0][0], outs[0][1], int(status.item())
+
+
+def check_batch(b, plan=None, target=None, override=None, check_partials=True, d=None, fused=True):
     plan = plan if plan is not None else make_plan(b, target, override)
+    d = d if d is not None else b.to("cuda")
     v, l, o, lo, st = run_gpu(b, plan, d)
     assert st == 0, f"{b.name}: device status {st}"
     ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                     b.first_page_offset, b.scale)
     errs = assert_close(o, lo, ref_o, ref_l, f"{b.name} merged (ppc={plan.pages_per_chunk})")
+    if fused:
+        fo, fl, fst = run_gpu_fused(b, plan, d)
+        assert fst == 0, f"{b.name}: fused device status {fst}"
+        assert_close(fo, fl, ref_o, ref_l, f"{b.name} fused (ppc={plan.pages_per_chunk})")
     if check_partials:
         pv, pl = oracle.partials(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                  b.first_page_offset, b.scale, plan.pages_per_chunk, plan.request_indices,
