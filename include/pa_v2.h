@@ -193,6 +193,39 @@ pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, const void* k_p
                        float sm_scale, float* workspace_v, float* workspace_lse, int32_t* counters, float* out,
                        float* lse2_out, int32_t* status, void* cuda_stream);
 
+/* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
+ * by every GPU that loads this library until the process exits. */
+#define PA_V2_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* pa_v2_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for users whose process
+ * does not let them call cudaMalloc: a serving engine that reserves all device
+ * memory up front for its own pools, or a plugin that is handed only input and
+ * output pointers by its host.  Such a caller cannot provide the partial
+ * workspace and ticket counters pa_v2_decode needs, so this call takes them
+ * from a fixed array in the library's own device memory
+ * (PA_V2_NOALLOC_SCRATCH_BYTES, laid out as counters, then workspace_v, then
+ * workspace_lse, each rounded up to 256 bytes).  It allocates nothing.
+ *  - The caller still passes every input and output (same arguments and
+ *    layouts as pa_v2_decode, minus workspace_v / workspace_lse / counters).
+ *  - A plan whose counters plus workspace exceed PA_V2_NOALLOC_SCRATCH_BYTES
+ *    is rejected with PA_ECAPACITY before anything is launched.
+ *  - The first call on a device looks up that device's copy of the array
+ *    (cudaGetSymbolAddress, with that device current) and remembers it; make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind.  Each call clears the counter region on its stream
+ *    (cudaMemsetAsync) before the launch.  Calls whose work overlaps on the GPU
+ *    (different streams, or no ordering between them) race on the array:
+ *    order them on one stream. */
+pa_status pa_v2_decode_noalloc(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
+                               const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                               const int32_t* indices, int64_t num_indices, const int32_t* indptr,
+                               const int32_t* last_page_len, const int32_t* first_page_offset,
+                               const int32_t* request_indices, const int32_t* kv_tile_indices,
+                               const int32_t* o_indptr, float sm_scale, float* out, float* lse2_out,
+                               int32_t* status, void* cuda_stream);
+
 /* The variable-length merge (issue #898, design piece 3 and Task 3; PR
  * #984, What changed 3).  For output row r and head h, the rows
  * o_indptr[r] .. o_indptr[r+1]-1 of (v_in, lse2_in) merge by

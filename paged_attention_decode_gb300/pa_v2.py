@@ -29,8 +29,9 @@ KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF
 
 # Exported symbols of the C ABI (the header's declarations).
 ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
-               "pa_v2_decode_partial", "pa_v2_decode", "pa_merge_states", "pa_status_from_device",
-               "pa_status_string", "pa_version")
+               "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
+               "pa_status_from_device", "pa_status_string", "pa_version")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class PaError(RuntimeError):
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_decode_partial.restype = i32
         L.pa_v2_decode.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P, P, P, P]
         L.pa_v2_decode.restype = i32
+        L.pa_v2_decode_noalloc.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P]
+        L.pa_v2_decode_noalloc.restype = i32
         L.pa_merge_states.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
         L.pa_merge_states.restype = i32
         L.pa_status_from_device.argtypes = [i32]
@@ -290,6 +293,36 @@ def pa_v2_decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, 
         _dev_ptr(status, "status", torch.int32), _stream(stream))
     if rc != PA_OK:
         raise PaError(rc, "pa_v2_decode")
+    return out[:s.batch], lse2_out[:s.batch]
+
+
+def pa_v2_decode_noalloc(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
+                         sm_scale: float, out=None, lse2_out=None, status=None, stream=None):
+    """pa_v2_decode for callers that cannot allocate device memory (pa_v2_decode_noalloc).
+
+    The partial workspace and the ticket counters come from the library's own fixed device array
+    (NOALLOC_SCRATCH_BYTES per GPU); the caller supplies every input and output.  Calls on one device
+    share that array, so keep them ordered on one stream.  Returns (out [B, Hq, D], lse2 [B, Hq]).
+    """
+    s = plan.struct
+    dev = q.device
+    ri, ti, oi = plan.device_arrays(dev)
+    if out is None:
+        out = torch.empty(max(s.batch, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(max(s.batch, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
+    rc = lib().pa_v2_decode_noalloc(
+        ctypes.byref(s), _dev_ptr(q, "q", torch.float32), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+        KV_DTYPES[k_pool.dtype], k_pool.shape[0], _dev_ptr(indices, "indices", torch.int32), indices.numel(),
+        _dev_ptr(indptr, "indptr", torch.int32), _dev_ptr(last_page_len, "last_page_len", torch.int32),
+        _dev_ptr(first_page_offset, "first_page_offset", torch.int32),
+        _dev_ptr(ri, "request_indices", torch.int32), _dev_ptr(ti, "kv_tile_indices", torch.int32),
+        _dev_ptr(oi, "o_indptr", torch.int32), float(sm_scale), _dev_ptr(out, "out", torch.float32),
+        _dev_ptr(lse2_out, "lse2_out", torch.float32), _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_decode_noalloc")
     return out[:s.batch], lse2_out[:s.batch]
 
 
