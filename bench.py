@@ -41,7 +41,6 @@ import torch  # noqa: E402
 
 METRIC = "decode KV-read GB/s (% of GB300 HBM peak) and µs/step at 32K context"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_v2_partial_llama3_8b_32k.md")
 
 
 def parse_args():
@@ -56,6 +55,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=32768)
+    ap.add_argument("--workload", default="llama3_8b_32k",
+                    choices=["llama3_8b_32k", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix",
+                             "tiny_csr"],
+                    help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
+                         "(cold L2 for every step)")
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
     ap.add_argument("--two-launch", action="store_true",
                     help="time pa_v2_decode_partial + pa_merge_states instead of the one-launch pa_v2_decode")
@@ -72,6 +76,21 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_over_ranks(ms_total: float, units: float, world: int, device=None):
+    """Max of the timed region over ranks and the sum of the units every rank processed.
+
+    With one rank this is the identity.  With several (torch.distributed already initialised), the
+    job's time is the slowest rank's and its throughput is all ranks' units over that time."""
+    if world <= 1:
+        return ms_total, units
+    import torch.distributed as dist
+    t = torch.tensor([ms_total, units], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(mx[0].item()), float(t[1].item())
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -81,18 +100,33 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(kernel_src: str):
-    """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel changed since."""
+KERNEL_SOURCES = {
+    "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_internal.cuh", "pa_device.cuh"],
+    "pa_v2_partial_simt_kernel": ["pa_partial_simt.cu", "pa_internal.cuh", "pa_device.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over the source files that define `kernel` (in KERNEL_SOURCES order)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "paged_attention_decode_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str):
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary of `kernel` on this workload,
+    or None when the kernel's sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel.replace('pa_v2_', '')}_llama3_8b_32k.md")
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(path).read()
     except OSError:
         return None
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     if not m_hash or not m_traffic:
         return None
-    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return int(m_traffic.group(1)) if cur == m_hash.group(1) else None
+    return int(m_traffic.group(1)) if kernel_source_hash(kernel) == m_hash.group(1) else None
 
 
 class ClockSampler:
@@ -363,11 +397,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, job_bytes = reduce_over_ranks(t_start.elapsed_time(t_end), float(kv_bytes) * args.steps, world, dev)
     ms_step = ms_total / args.steps
 
     # per-launch duration of the dominant (partial) kernel: a second timed region replaying a graph of
@@ -399,10 +429,10 @@ def run_ours(args):
     e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
 
     peak, peak_kind = measured_peak()
-    gbs = kv_bytes * world / (ms_step * 1e-3) / 1e9
+    gbs = job_bytes / (ms_total * 1e-3) / 1e9
     achieved = partial_bytes / (partial_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(os.path.join(ROOT, "paged_attention_decode_gb300", "csrc",
-                                       "pa_partial_simt.cu" if args.kernel == 1 else "pa_partial_tc.cu"))
+    kernel_name = "pa_v2_partial_simt_kernel" if args.kernel == 1 else "pa_v2_partial_tc_kernel"
+    traffic = ncu_traffic(kernel_name)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
@@ -417,7 +447,7 @@ def run_ours(args):
                          "between reuses of a set; L2 is 126 MB)",
                    "cuda_graph": bool(graph is not None), "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
-                     "kernel": "pa_v2_partial_simt_kernel" if args.kernel == 1 else "pa_v2_partial_tc_kernel", "achieved": achieved, "peak": peak,
+                     "kernel": kernel_name, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": partial_bytes, "launch_us": partial_ms * 1e3,
                      "rest_of_step_us": ms_step * 1e3 - partial_ms * 1e3,
@@ -479,10 +509,136 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
             "path": "pa_v2_plan_matches + pa_v2_decode via the ctypes binding"}
 
 
+def run_workload(args):
+    """Per-step timing of one of the other workloads: every step starts with a cold L2 (a 512 MiB
+    buffer is written between steps, outside the event pair), the step is the one-launch pa_v2_decode
+    (the cascade: level 0 + level 1 + one pa_merge_states, against the flat pa_v2_decode of the same batch)."""
+    from paged_attention_decode_gb300 import build as pa_build
+    from paged_attention_decode_gb300 import pa_v2 as pa
+    from paged_attention_decode_gb300 import workloads as W
+    import oracle
+
+    pa_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    cascade = args.workload == "cascade_shared_prefix"
+    cb = W.cascade_shared_prefix() if cascade else None
+    b = cb.flat if cascade else W.WORKLOADS[args.workload]()
+    dt = pa.KV_DTYPES[b.dtype]
+
+    def make_plan(indptr, lpl, fpo, hq, seq_lens=None, override=0):
+        tgt = pa.pa_v2_default_target_ctas(hq, b.num_kv_heads, b.head_dim, b.page_size, dt)
+        return pa.pa_v2_plan(indptr, lpl, fpo, b.page_size, hq, b.num_kv_heads, b.head_dim, dt, tgt, override,
+                             seq_lens)
+
+    d = b.to(dev)
+    plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, b.ppc_override)
+    out = torch.empty(b.batch, b.num_qo_heads, b.head_dim, device=dev)
+    lse = torch.empty(b.batch, b.num_qo_heads, device=dev)
+
+    def workspace(pl):
+        return (torch.empty(max(1, pl.num_chunks), pl.num_qo_heads, pl.head_dim, device=dev),
+                torch.empty(max(1, pl.num_chunks), pl.num_qo_heads, device=dev))
+
+    ws = workspace(plan)
+
+    def flat_step():
+        pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len, d.first_page_offset,
+                        b.scale, out, lse, ws, None, None, stream)
+
+    steps = {"flat": (flat_step, b.kv_bytes())}
+    if cascade:
+        M, Hq, D = b.q.shape
+        Hkv, G = b.num_kv_heads, Hq // b.num_kv_heads
+        npre = len(cb.prefix_indices)
+        ip0, lp0, fp0 = [torch.tensor(x, dtype=torch.int32) for x in ([0, npre], [b.page_size], [0])]
+        p0 = make_plan(ip0, lp0, fp0, M * Hq)
+        fp1 = torch.zeros(M, dtype=torch.int32)
+        p1 = make_plan(cb.suffix_indptr, cb.suffix_last_page_len, fp1, Hq)
+        pre_i, ip0d, lp0d, fp0d = [x.to(dev) for x in (cb.prefix_indices, ip0, lp0, fp0)]
+        suf_i, ip1d, lp1d, fp1d = [x.to(dev) for x in (cb.suffix_indices, cb.suffix_indptr, cb.suffix_last_page_len,
+                                                       fp1)]
+        q0 = torch.empty(1, M * Hq, D, device=dev)
+        o0 = torch.empty(1, M * Hq, D, device=dev)
+        l0 = torch.empty(1, M * Hq, device=dev)
+        o1 = torch.empty(M, Hq, D, device=dev)
+        l1 = torch.empty(M, Hq, device=dev)
+        v_in = torch.empty(M, 2, Hq, D, device=dev)
+        lse_in = torch.empty(M, 2, Hq, device=dev)
+        oi = torch.arange(0, 2 * M + 1, 2, dtype=torch.int32, device=dev)
+        c_out = torch.empty(M, Hq, D, device=dev)
+        c_lse = torch.empty(M, Hq, device=dev)
+        ws0, ws1 = workspace(p0), workspace(p1)
+
+        def cascade_step():
+            with torch.cuda.stream(stream):
+                # level 0: members' heads stacked h0 = kv*(M*G) + m*G + g (cascade-attention.md)
+                q0.view(Hkv, M, G, D).copy_(d.q.view(M, Hkv, G, D).permute(1, 0, 2, 3))
+                pa.pa_v2_decode(p0, q0, d.k_pool, d.v_pool, pre_i, ip0d, lp0d, fp0d, b.scale, o0, l0, ws0, None,
+                                None, stream)
+                pa.pa_v2_decode(p1, d.q, d.k_pool, d.v_pool, suf_i, ip1d, lp1d, fp1d, b.scale, o1, l1, ws1, None,
+                                None, stream)
+                v_in[:, 0].copy_(o0.view(Hkv, M, G, D).permute(1, 0, 2, 3).reshape(M, Hq, D))
+                lse_in[:, 0].copy_(l0.view(Hkv, M, G).permute(1, 0, 2).reshape(M, Hq))
+                v_in[:, 1].copy_(o1)
+                lse_in[:, 1].copy_(l1)
+                pa.pa_merge_states(v_in.view(2 * M, Hq, D), lse_in.view(2 * M, Hq), oi, M, c_out, c_lse, None, stream)
+
+        cas_bytes = (npre * b.page_size + sum(cb.suffix_lens)) * Hkv * D * 2 * b.k_pool.element_size()
+        steps["cascade"] = (cascade_step, cas_bytes)
+
+    # correctness guard before timing
+    ref_o, _ = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                b.first_page_offset, b.scale)
+    with torch.cuda.stream(stream):
+        flat_step()
+        if cascade:
+            steps["cascade"][0]()
+    stream.synchronize()
+    for name, got in (("flat", out),) + ((("cascade", c_out),) if cascade else ()):
+        err = float(abs(got.cpu().double().numpy() - ref_o).max())
+        if err > 2e-3:
+            raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}); refusing to time")
+
+    res = {}
+    for name, (fn, nbytes) in steps.items():
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.fill_(i & 0xff)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                times.append((e0, e1))
+        stream.synchronize()
+        t = sorted(a.elapsed_time(z) for a, z in times[args.warmup:])
+        med = t[len(t) // 2]
+        res[name] = {"us_per_step_median": med * 1e3, "us_p10": t[len(t) // 10] * 1e3,
+                     "us_p90": t[(9 * len(t)) // 10] * 1e3, "kv_bytes_per_step": nbytes,
+                     "kv_read_gbs": nbytes / (med * 1e-3) / 1e9}
+    peak, peak_kind = measured_peak()
+    main = res["cascade" if cascade else "flat"]
+    line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main["us_per_step_median"],
+            "unit": "us/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+                       "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
+                       "kv_dtype": str(b.dtype).replace("torch.", ""), "seq_lens_total": sum(b.seq_lens),
+                       "num_chunks": plan.num_chunks, "pages_per_chunk": plan.pages_per_chunk,
+                       "l2": "512 MiB buffer written between steps"},
+            "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "llama3_8b_32k":
+        run_workload(args)
     else:
         run_ours(args)
 
