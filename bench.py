@@ -464,36 +464,46 @@ def run_ours(args):
 
 
 def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
-    """Per step: pinned H2D of q and the page table, plan check, kernels, D2H of out + lse, sync."""
+    """Per step: one pinned H2D copy of q and the page table, the cached plan checked with
+    pa_v2_plan_matches, pa_v2_decode, one D2H copy of out + lse, stream sync."""
     B, Hq, D = b0.batch, b0.num_qo_heads, b0.head_dim
-    host_in = []
+    # one pinned staging buffer per input set: [q (f32) | indices | indptr | lpl | fpo] as 32-bit words
+    host_in, views = [], []
     for b in sets_cpu:
-        host_in.append([t.pin_memory() for t in (b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)])
-    dev_in = [[torch.empty_like(t, device=dev) for t in h] for h in host_in]
-    out_h = torch.empty(B, Hq, D).pin_memory()
-    lse_h = torch.empty(B, Hq).pin_memory()
+        parts = [b.q.reshape(-1).view(torch.int32), b.indices, b.indptr, b.last_page_len, b.first_page_offset]
+        buf = torch.cat([p.reshape(-1).to(torch.int32) for p in parts]).pin_memory()
+        host_in.append((buf, b))
+    dev_in = torch.empty(max(h[0].numel() for h in host_in), dtype=torch.int32, device=dev)
+    n_q = B * Hq * D
+    res_h = torch.empty(B * Hq * (D + 1), dtype=torch.float32).pin_memory()
+    res_d = torch.empty(B * Hq * (D + 1), dtype=torch.float32, device=dev)
+    out = res_d[:B * Hq * D].view(B, Hq, D)
+    lse = res_d[B * Hq * D:].view(B, Hq)
     wv = torch.empty(plan.num_chunks, Hq, D, device=dev)
     wl = torch.empty(plan.num_chunks, Hq, device=dev)
-    out = torch.empty(B, Hq, D, device=dev)
-    lse = torch.empty(B, Hq, device=dev)
     ri, ti, oi = plan.device_arrays(dev)
     counters = plan.device_counters(dev)
-    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    h2d = host_in[0][0].numel() * 4
+    d2h = res_h.numel() * 4
 
     def one(i):
-        k = i % len(sets)
-        hi, di = host_in[k], dev_in[k]
-        if not pa.pa_v2_plan_matches(plan, hi[2], hi[3], hi[4]):
+        buf, b = host_in[i % len(host_in)]
+        if not pa.pa_v2_plan_matches(plan, b.indptr, b.last_page_len, b.first_page_offset):
             raise RuntimeError("plan no longer matches")
+        nnz = b.indices.numel()
         with torch.cuda.stream(stream):
-            for src, dst in zip(hi, di):
-                dst.copy_(src, non_blocking=True)
-            q, idx, ip, lp, fp = di
-            pa.pa_v2_decode(plan, q, sets[k].k_pool, sets[k].v_pool, idx, ip, lp, fp, b0.scale, out, lse, (wv, wl),
-                            counters, None, stream, ri, ti, oi)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+            dev_in[:buf.numel()].copy_(buf, non_blocking=True)
+            q = dev_in[:n_q].view(torch.float32).view(B, Hq, D)
+            o = n_q
+            idx = dev_in[o:o + nnz]
+            o += nnz
+            ip = dev_in[o:o + B + 1]
+            o += B + 1
+            lp = dev_in[o:o + B]
+            fp = dev_in[o + B:o + 2 * B]
+            pa.pa_v2_decode(plan, q, sets[i % len(sets)].k_pool, sets[i % len(sets)].v_pool, idx, ip, lp, fp,
+                            b0.scale, out, lse, (wv, wl), counters, None, stream, ri, ti, oi)
+            res_h.copy_(res_d, non_blocking=True)
         stream.synchronize()
 
     for i in range(20):
@@ -506,13 +516,15 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     kv_bytes = b0.kv_bytes()
     return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pa_v2_plan_matches + pa_v2_decode via the ctypes binding"}
+            "path": "per step: 1 pinned H2D (q + page table), pa_v2_plan_matches, pa_v2_decode, 1 D2H (out + lse), "
+                    "stream sync; ctypes binding"}
 
 
 def run_workload(args):
     """Per-step timing of one of the other workloads: every step starts with a cold L2 (a 512 MiB
-    buffer is written between steps, outside the event pair), the step is the one-launch pa_v2_decode
-    (the cascade: level 0 + level 1 + one pa_merge_states, against the flat pa_v2_decode of the same batch)."""
+    buffer is read between steps, outside the event pair), the step is the one-launch pa_v2_decode
+    (the cascade: level 0 + level 1 + one pa_merge_states, against the flat pa_v2_decode of the same batch).
+    The buffer is read, not written, so no dirty lines are written back during the step."""
     from paged_attention_decode_gb300 import build as pa_build
     from paged_attention_decode_gb300 import pa_v2 as pa
     from paged_attention_decode_gb300 import workloads as W
@@ -522,7 +534,7 @@ def run_workload(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)   # 512 MiB, read between steps
     cascade = args.workload == "cascade_shared_prefix"
     cb = W.cascade_shared_prefix() if cascade else None
     b = cb.flat if cascade else W.WORKLOADS[args.workload]()
@@ -589,6 +601,15 @@ def run_workload(args):
         cas_bytes = (npre * b.page_size + sum(cb.suffix_lens)) * Hkv * D * 2 * b.k_pool.element_size()
         steps["cascade"] = (cascade_step, cas_bytes)
 
+    if args.profile:
+        with torch.cuda.stream(stream):
+            for _ in range(args.profile):
+                for fn, _ in steps.values():
+                    fn()
+        stream.synchronize()
+        print(f"profile mode: {args.workload}, {args.profile} steps of {list(steps)}", flush=True)
+        return
+
     # correctness guard before timing
     ref_o, _ = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                 b.first_page_offset, b.scale)
@@ -607,7 +628,7 @@ def run_workload(args):
         times = []
         with torch.cuda.stream(stream):
             for i in range(args.warmup + args.steps):
-                flush.fill_(i & 0xff)
+                flush.sum()   # reads 512 MiB: the next step starts with a cold, clean L2
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 fn()
@@ -628,7 +649,7 @@ def run_workload(args):
                        "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
                        "kv_dtype": str(b.dtype).replace("torch.", ""), "seq_lens_total": sum(b.seq_lens),
                        "num_chunks": plan.num_chunks, "pages_per_chunk": plan.pages_per_chunk,
-                       "l2": "512 MiB buffer written between steps"},
+                       "l2": "512 MiB buffer read between steps"},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
     print(json.dumps(line), flush=True)
 

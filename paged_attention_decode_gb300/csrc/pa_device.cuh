@@ -85,6 +85,13 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled now (it still waits for this grid's completion before touching
+// memory), and, in a kernel launched as a dependent, wait until the grids it
+// depends on have completed and their writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -47,6 +47,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   __shared__ float wsum_s[kMergeWarps];
   __shared__ __align__(16) float acc_s[kMergeWarps][128];
 
+  // launched as a programmatic dependent of the partial kernel: wait for its
+  // grid to complete (and its writes to be visible) before reading anything
+  pdl_wait_prerequisites();
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x / num_heads;
@@ -143,12 +147,23 @@ extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, co
   if (vec && (((uintptr_t)v_in | (uintptr_t)v_out) & 15u)) return PA_EINVAL;
   const long long blocks = (long long)num_rows_out * num_heads;
   if (blocks > 0x7fffffffLL) return PA_EUNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (vec)
-    pa::pa_merge_states_kernel<true><<<(unsigned)blocks, pa::kMergeWarps * 32, 0, s>>>(
-        v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status);
-  else
-    pa::pa_merge_states_kernel<false><<<(unsigned)blocks, pa::kMergeWarps * 32, 0, s>>>(
-        v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+  // Programmatic dependent launch: the merge may be scheduled while the kernel
+  // before it in the stream (normally the partial kernel) is still running; the
+  // kernel's first instruction waits for that grid to complete.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(pa::kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t rc = vec ? cudaLaunchKernelEx(&cfg, pa::pa_merge_states_kernel<true>, v_in, lse2_in, o_indptr,
+                                            num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status)
+                       : cudaLaunchKernelEx(&cfg, pa::pa_merge_states_kernel<false>, v_in, lse2_in, o_indptr,
+                                            num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out,
+                                            status);
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
 }

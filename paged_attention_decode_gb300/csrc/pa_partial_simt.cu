@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int nheads = min(p.hpc, p.group - qg * p.hpc);
   const int ps = p.page_size;
 
+  // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+  pdl_launch_dependents();
+
   // ---- chunk geometry ----
   int r;
   const ChunkGeom g = chunk_geom(p, c, &r);

@@ -165,6 +165,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int nheads = min(p.hpc, p.group - qg * p.hpc);
   const int ps = p.page_size;
 
+  // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+  pdl_launch_dependents();
+
   int r;
   const ChunkGeom gm = chunk_geom(p, c, &r);
 
