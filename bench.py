@@ -61,6 +61,8 @@ def parse_args():
                     help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
                          "(cold L2 for every step)")
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
+    ap.add_argument("--tune", action="store_true",
+                    help="--workload runs: also time the chunk size picked by the autotuner")
     ap.add_argument("--two-launch", action="store_true",
                     help="time pa_v2_decode_partial + pa_merge_states instead of the one-launch pa_v2_decode")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
@@ -547,6 +549,13 @@ def run_workload(args):
 
     d = b.to(dev)
     plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, b.ppc_override)
+    tuned = None
+    if args.tune and not cascade:
+        from paged_attention_decode_gb300 import autotune
+        tuned = autotune.tune(b, dev, reps=20, stream=stream)
+        if tuned.pages_per_chunk != plan.pages_per_chunk:
+            plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens,
+                             tuned.pages_per_chunk)
     out = torch.empty(b.batch, b.num_qo_heads, b.head_dim, device=dev)
     lse = torch.empty(b.batch, b.num_qo_heads, device=dev)
 
@@ -562,41 +571,23 @@ def run_workload(args):
 
     steps = {"flat": (flat_step, b.kv_bytes())}
     if cascade:
+        from paged_attention_decode_gb300 import cascade as C
         M, Hq, D = b.q.shape
         Hkv, G = b.num_kv_heads, Hq // b.num_kv_heads
         npre = len(cb.prefix_indices)
-        ip0, lp0, fp0 = [torch.tensor(x, dtype=torch.int32) for x in ([0, npre], [b.page_size], [0])]
-        p0 = make_plan(ip0, lp0, fp0, M * Hq)
         fp1 = torch.zeros(M, dtype=torch.int32)
-        p1 = make_plan(cb.suffix_indptr, cb.suffix_last_page_len, fp1, Hq)
-        pre_i, ip0d, lp0d, fp0d = [x.to(dev) for x in (cb.prefix_indices, ip0, lp0, fp0)]
-        suf_i, ip1d, lp1d, fp1d = [x.to(dev) for x in (cb.suffix_indices, cb.suffix_indptr, cb.suffix_last_page_len,
-                                                       fp1)]
-        q0 = torch.empty(1, M * Hq, D, device=dev)
-        o0 = torch.empty(1, M * Hq, D, device=dev)
-        l0 = torch.empty(1, M * Hq, device=dev)
-        o1 = torch.empty(M, Hq, D, device=dev)
-        l1 = torch.empty(M, Hq, device=dev)
-        v_in = torch.empty(M, 2, Hq, D, device=dev)
-        lse_in = torch.empty(M, 2, Hq, device=dev)
-        oi = torch.arange(0, 2 * M + 1, 2, dtype=torch.int32, device=dev)
+        t0 = pa.pa_v2_default_target_ctas(M * Hq, Hkv, D, b.page_size, dt)
+        t1 = pa.pa_v2_default_target_ctas(Hq, Hkv, D, b.page_size, dt)
+        cplan = C.cascade_plan(npre, cb.suffix_indptr, cb.suffix_last_page_len, fp1, b.page_size, Hq, Hkv, D, dt,
+                               t0, t1, cb.suffix_lens)
+        c_args = (d.q, d.k_pool, d.v_pool, cb.prefix_indices.to(dev), cb.suffix_indices.to(dev),
+                  cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev), fp1.to(dev), b.scale)
         c_out = torch.empty(M, Hq, D, device=dev)
         c_lse = torch.empty(M, Hq, device=dev)
-        ws0, ws1 = workspace(p0), workspace(p1)
 
         def cascade_step():
-            with torch.cuda.stream(stream):
-                # level 0: members' heads stacked h0 = kv*(M*G) + m*G + g (cascade-attention.md)
-                q0.view(Hkv, M, G, D).copy_(d.q.view(M, Hkv, G, D).permute(1, 0, 2, 3))
-                pa.pa_v2_decode(p0, q0, d.k_pool, d.v_pool, pre_i, ip0d, lp0d, fp0d, b.scale, o0, l0, ws0, None,
-                                None, stream)
-                pa.pa_v2_decode(p1, d.q, d.k_pool, d.v_pool, suf_i, ip1d, lp1d, fp1d, b.scale, o1, l1, ws1, None,
-                                None, stream)
-                v_in[:, 0].copy_(o0.view(Hkv, M, G, D).permute(1, 0, 2, 3).reshape(M, Hq, D))
-                lse_in[:, 0].copy_(l0.view(Hkv, M, G).permute(1, 0, 2).reshape(M, Hq))
-                v_in[:, 1].copy_(o1)
-                lse_in[:, 1].copy_(l1)
-                pa.pa_merge_states(v_in.view(2 * M, Hq, D), lse_in.view(2 * M, Hq), oi, M, c_out, c_lse, None, stream)
+            # level 0 (stacked heads, read in place) + level 1 + one merge: three launches
+            C.cascade_decode(cplan, *c_args, out=c_out, lse2_out=c_lse, stream=stream)
 
         cas_bytes = (npre * b.page_size + sum(cb.suffix_lens)) * Hkv * D * 2 * b.k_pool.element_size()
         steps["cascade"] = (cascade_step, cas_bytes)
@@ -651,6 +642,10 @@ def run_workload(args):
                        "num_chunks": plan.num_chunks, "pages_per_chunk": plan.pages_per_chunk,
                        "l2": "512 MiB buffer read between steps"},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
+    if tuned is not None:
+        line["autotune"] = {"pages_per_chunk": tuned.pages_per_chunk, "default": tuned.default_pages_per_chunk,
+                            "times_us": {str(k): round(v, 2) for k, v in tuned.times_us.items()},
+                            "num_chunks": {str(k): v for k, v in tuned.num_chunks.items()}}
     print(json.dumps(line), flush=True)
 
 

@@ -93,6 +93,16 @@ typedef struct pa_v2_plan_t {
     int32_t kernel;                   /* 0: tensor cores for f16/bf16 pools, CUDA cores for f32;
                                          1: CUDA cores (needs q_heads_per_cta <= 8).  Set by the
                                          caller after pa_v2_plan; pa_v2_plan writes 0. */
+    int32_t stack_members;            /* Cascade level 0 (cascade-attention.md): when M > 1 the plan's
+                                         single request holds the query heads of M members stacked
+                                         h0 = kv*(M*Gm) + m*Gm + g (Gm = num_qo_heads / (M *
+                                         num_kv_heads)); q is read, and pa_v2_decode's out / lse2 are
+                                         written, in member layout [M, Hm, D] / [M, Hm].  Set by the
+                                         caller; pa_v2_plan writes 1. */
+    int32_t out_row_step;             /* pa_v2_decode writes final row r (request, or member when
+                                         stacked) at row r * out_row_step of out / lse2, so two
+                                         decodes can fill interleaved rows for one pa_merge_states.
+                                         pa_v2_plan writes 1. */
     int64_t num_indices;              /* indptr[batch] */
     int64_t workspace_v_bytes;        /* num_chunks * num_qo_heads * head_dim * 4 */
     int64_t workspace_lse_bytes;      /* num_chunks * num_qo_heads * 4 */
@@ -184,6 +194,12 @@ pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const v
  *                 first call; the kernel leaves them zero.  After a call that
  *                 failed on the device (status word non-zero), zero them again.
  *   out [batch, num_qo_heads, head_dim] f32, lse2_out [batch, num_qo_heads] f32.
+ *   member_rows   nullable device int32 [stack_members]: for a stacked plan,
+ *                 the q row group (request) of member m; null means m.
+ *   out_rows      nullable device int32 [batch, or stack_members when stacked]:
+ *                 the row of out / lse2 that request (member) r is written to;
+ *                 null means r * plan->out_row_step.  (pa_v2_cascade_split
+ *                 produces both maps for a mixed cascade batch.)
  * Other arguments, layouts and errors as pa_v2_decode_partial.  Two calls
  * sharing `counters` must not overlap on the GPU. */
 pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
@@ -191,7 +207,40 @@ pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, const void* k_p
                        const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
                        const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
                        float sm_scale, float* workspace_v, float* workspace_lse, int32_t* counters, float* out,
-                       float* lse2_out, int32_t* status, void* cuda_stream);
+                       float* lse2_out, const int32_t* member_rows, const int32_t* out_rows, int32_t* status,
+                       void* cuda_stream);
+
+/* Shared-prefix detection for cascade decode (cascade-attention.md, the
+ * detection paragraphs and their table).  Requests with first_page_offset != 0
+ * or fewer than 2 pages are left out; the rest are grouped by their first page
+ * id; a group's shared span is the number of leading page positions on which
+ * all members hold the same page id, capped at pages - 1 for every member; the
+ * group with the largest shared * (members - 1) wins (ties: the group whose
+ * first member comes first).  It is reported only with at least
+ * max(2, min_members) members and min_shared_pages shared pages; otherwise
+ * *num_members = 0.  HOST pointers: indptr [batch+1], indices [indptr[batch]],
+ * first_page_offset [batch]; member_of [batch] receives 1 for members, 0 else. */
+pa_status pa_v2_cascade_detect(const int32_t* indptr, const int32_t* indices,
+                               const int32_t* first_page_offset, int32_t batch,
+                               int32_t min_shared_pages, int32_t min_members, int32_t* member_of,
+                               int32_t* num_members, int32_t* shared_pages);
+
+/* Split a batch into the two cascade levels (cascade-attention.md).  Level 0
+ * is the first `shared_pages` pages of the members (all full), attended once
+ * with the members' heads stacked; level 1 is every request's remaining pages
+ * (members: after the shared span; others: all of them).  The merge input has
+ * one row group per request: members two rows (level 0 first, level 1 second),
+ * others one row.  HOST pointers.  Outputs: l1_indptr [batch+1], l1_indices
+ * [indptr[batch] - members * shared_pages], l1_last_page_len / l1_first_page_offset
+ * [batch], member_rows [members] (request of member m, batch order),
+ * l0_out_rows [members] and l1_out_rows [batch] (merge-input rows written by
+ * level 0 / level 1, for pa_v2_decode's out_rows), merge_indptr [batch+1]. */
+pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
+                              const int32_t* first_page_offset, int32_t batch, const int32_t* member_of,
+                              int32_t shared_pages, int32_t* l1_indptr, int32_t* l1_indices,
+                              int32_t* l1_last_page_len, int32_t* l1_first_page_offset,
+                              int32_t* member_rows, int32_t* l0_out_rows, int32_t* l1_out_rows,
+                              int32_t* merge_indptr);
 
 /* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
  * by every GPU that loads this library until the process exits. */

@@ -11,6 +11,7 @@ Cascade composition (``cascade_ref``) follows cascade-attention.md (issue
 #903): level 0 attends the shared span once with the members' query heads
 stacked ``h0 = kv * (M * G) + m * G + g``, level 1 attends each member's
 private suffix, and one merge pairs each member's two states.
+``cascade_detect_ref`` is that page's detection rule written as plain loops.
 """
 from __future__ import annotations
 
@@ -269,3 +270,46 @@ def cascade_ref(q, k_pool, v_pool, prefix_indices, suffix_indices, suffix_indptr
     v_in = torch.stack([o0, torch.from_numpy(o1)], dim=1).reshape(2 * M, Hq, D)
     lse_in = torch.stack([l0, torch.from_numpy(l1)], dim=1).reshape(2 * M, Hq)
     return merge(v_in, lse_in, list(range(0, 2 * M + 1, 2)))
+
+
+def cascade_detect_ref(indptr, indices, first_page_offset, min_shared_pages: int = 16, min_members: int = 2):
+    """Shared-prefix detection (cascade-attention.md, issue #903, the detection paragraphs and table).
+
+    Requests whose window starts mid-page are left out.  The rest are grouped by their first page id;
+    a group's shared span is the number of leading page positions on which all its members hold the
+    same page id, capped at (pages - 1) for every member (a last page may be partly filled); its score is
+    shared * (members - 1), the page reads it removes.  The best-scoring group wins (on a tie, the group
+    whose first member comes first in the batch).  It is used only if it has at least `min_members`
+    members and `min_shared_pages` shared pages.  Returns (members: sorted request list, shared_pages);
+    ([], 0) when nothing qualifies.
+    """
+    ip = [int(x) for x in _i32(indptr)]
+    idx = [int(x) for x in _i32(indices)]
+    fp = [int(x) for x in _i32(first_page_offset)]
+    B = len(ip) - 1
+    groups = {}
+    order = []
+    for r in range(B):
+        pages = ip[r + 1] - ip[r]
+        if fp[r] != 0 or pages < 2:
+            continue
+        key = idx[ip[r]]
+        if key not in groups:
+            groups[key] = []
+            order.append(key)
+        groups[key].append(r)
+    best, best_score, best_shared = [], -1, 0
+    for key in order:
+        mem = groups[key]
+        if len(mem) < 2:
+            continue
+        cap = min(ip[r + 1] - ip[r] - 1 for r in mem)
+        shared = 0
+        while shared < cap and all(idx[ip[r] + shared] == idx[ip[mem[0]] + shared] for r in mem):
+            shared += 1
+        score = shared * (len(mem) - 1)
+        if score > best_score:
+            best, best_score, best_shared = mem, score, shared
+    if len(best) < max(2, min_members) or best_shared < min_shared_pages:
+        return [], 0
+    return list(best), best_shared

@@ -36,6 +36,14 @@ struct PartialParams {
   float* out;          // [batch, Hq, D]
   float* lse_final;    // [batch, Hq]
   int32_t fused;
+  // cascade level 0 (cascade-attention.md): M members' query heads stacked as one request,
+  // h0 = kv * (M * Gm) + m * Gm + g; q and the final output stay in member layout [M, Hm, D]
+  int32_t stack_members;   // M (1: no stacking)
+  int32_t member_group;    // Gm = query heads per KV head of one member
+  int32_t member_heads;    // Hm = query heads of one member
+  int32_t out_row_step;    // final output row r is written at row r * out_row_step
+  const int32_t* member_rows;  // stacked plans: request (q row group) of member m, or null for m
+  const int32_t* out_rows;     // final output row of request r (member m when stacked), or null
   int64_t num_pages;
   int64_t num_indices;
   int32_t batch;
@@ -68,6 +76,31 @@ struct FastDiv {
 
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t magic, uint32_t shift) {
   return (__umulhi(magic, n) + n) >> shift;
+}
+
+// Row of q (in units of head_dim) that serves query head h of request r.
+__device__ __forceinline__ size_t q_row(const PartialParams& p, int r, int h) {
+  if (p.stack_members > 1) {
+    const int within = h % p.group;  // position inside the KV head's stacked group
+    const int m = within / p.member_group;
+    const int hm = (h / p.group) * p.member_group + within % p.member_group;
+    const int req = p.member_rows ? p.member_rows[m] : m;
+    return (size_t)req * p.member_heads + hm;
+  }
+  return (size_t)r * p.num_qo_heads + h;
+}
+
+// Row of the final output / lse (in units of head_dim / 1) for query head h of request r.
+__device__ __forceinline__ size_t out_row(const PartialParams& p, int r, int h) {
+  if (p.stack_members > 1) {
+    const int within = h % p.group;
+    const int m = within / p.member_group;
+    const int hm = (h / p.group) * p.member_group + within % p.member_group;
+    const size_t row = p.out_rows ? (size_t)p.out_rows[m] : (size_t)m * p.out_row_step;
+    return row * p.member_heads + hm;
+  }
+  const size_t row = p.out_rows ? (size_t)p.out_rows[r] : (size_t)r * p.out_row_step;
+  return row * p.num_qo_heads + h;
 }
 
 struct ChunkGeom {
@@ -147,13 +180,14 @@ __device__ __forceinline__ StageGeom stage_geom(const ChunkGeom& g, int j, int p
 }
 
 // Merge the per-warp online-softmax states of a CTA of NW warps and write the
-// chunk's normalized output and lse2 to row `row` of (v_dst, lse_dst).  ms/ls:
+// chunk's normalized output and lse2: to workspace row `row` (a chunk), or,
+// when final_output, to the final output of request `row`.  ms/ls:
 // [NW][HP]; accs: [NW][HP][D] (unnormalized, relative to each warp's max).
 // Called by all threads after a __syncthreads() that follows the state writes.
 template <int HP, int D, int NW>
 __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, const float* ms, const float* ls,
-                                                        const float* accs, size_t row, int h_first, int nheads,
-                                                        float* v_dst, float* lse_dst) {
+                                                        const float* accs, int row, int h_first, int nheads,
+                                                        bool final_output) {
   for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
     const int h = idx / D;
     const int d = idx % D;
@@ -172,9 +206,15 @@ __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, 
       out = A / L;
       lse = M + fast_log2(L);
     }
-    const size_t o = row * p.num_qo_heads + h_first + h;
-    v_dst[o * D + d] = out;
-    if (d == 0) lse_dst[o] = lse;
+    if (final_output) {
+      const size_t o = out_row(p, row, h_first + h);
+      p.out[o * D + d] = out;
+      if (d == 0) p.lse_final[o] = lse;
+    } else {
+      const size_t o = (size_t)row * p.num_qo_heads + h_first + h;
+      p.v_out[o * D + d] = out;
+      if (d == 0) p.lse_out[o] = lse;
+    }
   }
 }
 
@@ -301,8 +341,9 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, float* scrat
         o = make_float4(acc.x / W, acc.y / W, acc.z / W, acc.w / W);
         lse = m + fast_log2(W);
       }
-      reinterpret_cast<float4*>(p.out + ((size_t)r * hq + head) * D)[quad] = o;
-      if (quad == 0) p.lse_final[(size_t)r * hq + head] = lse;
+      const size_t orow = out_row(p, r, head);
+      reinterpret_cast<float4*>(p.out + orow * D)[quad] = o;
+      if (quad == 0) p.lse_final[orow] = lse;
     }
   }
 }
@@ -320,10 +361,7 @@ __device__ __forceinline__ void finish_chunk(const PartialParams& p, const Chunk
     const int n0 = p.o_indptr[r], n1 = p.o_indptr[r + 1];
     direct = n1 - n0 == 1;
   }
-  if (direct)
-    combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, (size_t)r, h_first, nheads, p.out, p.lse_final);
-  else
-    combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, (size_t)c, h_first, nheads, p.v_out, p.lse_out);
+  combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, direct ? r : c, h_first, nheads, direct);
   if (p.fused && !g.bad && !direct) {
     __syncthreads();  // scratch aliases the state arrays just read
     fused_merge<D, NW>(p, scratch, r, h_first, nheads, gridDim.x);

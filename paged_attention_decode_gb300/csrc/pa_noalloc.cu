@@ -77,5 +77,5 @@ extern "C" pa_status pa_v2_decode_noalloc(const pa_v2_plan_t* plan, const float*
     return PA_ECUDA;
   return pa_v2_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr, last_page_len,
                       first_page_offset, request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v,
-                      workspace_lse, counters, out, lse2_out, status, cuda_stream);
+                      workspace_lse, counters, out, lse2_out, nullptr, nullptr, status, cuda_stream);
 }

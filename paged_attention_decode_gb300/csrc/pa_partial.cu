@@ -126,6 +126,8 @@ struct FusedArgs {
   int32_t* counters;
   float* out;
   float* lse_final;
+  const int32_t* member_rows;
+  const int32_t* out_rows;
 };
 
 pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
@@ -150,6 +152,9 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
   if (num_pages * (int64_t)ps >= (1ll << 31)) return PA_EUNSUPPORTED;
   const int hpc = pa_v2_q_heads_per_cta(plan->num_qo_heads / plan->num_kv_heads, D, kv_dtype);
   if (hpc != plan->q_heads_per_cta) return PA_EINVAL;
+  const int M = plan->stack_members;
+  if (M < 1 || plan->out_row_step < 1) return PA_EINVAL;
+  if (M > 1 && (plan->batch != 1 || plan->num_qo_heads % (M * plan->num_kv_heads) != 0)) return PA_EINVAL;
   const bool tc = pa::use_tensor_cores(kv_dtype, plan->kernel);
   if (!tc && hpc > 8) return PA_EUNSUPPORTED;
   const bool tma = !tc || pa::tc_uses_tma(ps);
@@ -186,6 +191,8 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
     p.counters = fused->counters;
     p.out = fused->out;
     p.lse_final = fused->lse_final;
+    p.member_rows = fused->member_rows;
+    p.out_rows = fused->out_rows;
     p.fused = 1;
   }
   p.num_pages = num_pages;
@@ -202,6 +209,10 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
   p.ps_magic = fd.magic;
   p.ps_shift = fd.shift;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.stack_members = M;
+  p.member_heads = plan->num_qo_heads / M;
+  p.member_group = p.group / M;
+  p.out_row_step = plan->out_row_step;
   a.tm_k = &tm_k;
   a.tm_v = &tm_v;
   a.kv_dtype = kv_dtype;
@@ -231,8 +242,9 @@ extern "C" pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, cons
                                   const int32_t* first_page_offset, const int32_t* request_indices,
                                   const int32_t* kv_tile_indices, const int32_t* o_indptr, float sm_scale,
                                   float* workspace_v, float* workspace_lse, int32_t* counters, float* out,
-                                  float* lse2_out, int32_t* status, void* cuda_stream) {
-  const FusedArgs f{o_indptr, counters, out, lse2_out};
+                                  float* lse2_out, const int32_t* member_rows, const int32_t* out_rows,
+                                  int32_t* status, void* cuda_stream) {
+  const FusedArgs f{o_indptr, counters, out, lse2_out, member_rows, out_rows};
   return launch_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr, last_page_len,
                        first_page_offset, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse,
                        status, cuda_stream, &f);

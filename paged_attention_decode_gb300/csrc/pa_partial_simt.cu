@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
   for (int h = 0; h < HP; ++h) {
     if (h < nheads) {
-      const float* qp = p.q + ((size_t)r * p.num_qo_heads + h_first + h) * D + dl * VEC;
+      const float* qp = p.q + q_row(p, r, h_first + h) * D + dl * VEC;
 #pragma unroll
       for (int e = 0; e < VEC; e += 4) {
         float4 v = *reinterpret_cast<const float4*>(qp + e);

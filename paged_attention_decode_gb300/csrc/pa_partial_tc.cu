@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(NW * 32)
                             const PartialParams p) {
   using L = TcLayout<D, NT, NSW, NW>;
   constexpr int HP = L::HP;
+  // EARLY: copy a stage's K and V fragments to registers and release its slot
+  // before the math.  Measured slower on GB300 (26.9 vs 26.1 us on the 32K
+  // decode, same GPU), so the slot is released after the math.
+  constexpr bool EARLY = false;
   constexpr int KSTEPS = D / 16;
   constexpr int CPR = D / 8;  // 16-byte chunks per K/V row
 
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(NW * 32)
   for (int j = 0; j < NT; ++j) {
     const int head = 8 * j + g;
     const bool ok = head < nheads;
-    const float* qp = p.q + ((size_t)r * p.num_qo_heads + h_first + (ok ? head : 0)) * D + 2 * t;
+    const float* qp = p.q + q_row(p, r, h_first + (ok ? head : 0)) * D + 2 * t;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       float x[4];
@@ -323,25 +327,62 @@ __global__ void __launch_bounds__(NW * 32)
     unsigned char* vt = kt + L::TILE;
     const uint32_t kbase = smem_addr(kt);
     const uint32_t vbase = smem_addr(vt);
+    const int krow = ((lane >> 3) & 1) * 8 + (lane & 7);  // K fragment row this lane addresses
+    const int vtok = (lane >> 4) * 8 + (lane & 7);        // V^T fragment token this lane addresses
 
-    // ---- S^T = K . Q^T (hi and lo halves in separate accumulators) ----
-    float sh[NT][4], sl[NT][4];
+    // rows of the V tile outside [lo, hi) may hold stale or non-finite data: zero them
+    if (sg.lo > 0 || sg.hi < kStageRows) {
+      for (int idx = lane; idx < kStageRows * CPR; idx += 32) {
+        const int row = idx / CPR;
+        if (row < sg.lo || row >= sg.hi)
+          *reinterpret_cast<uint4*>(vt + (idx % CPR >> 3) * 2048 + row * 128 + (idx % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+
+    // Refill this slot with the warp's stage NSW rounds ahead (after the math,
+    // or, with EARLY, once the stage's fragments are in registers).
+    auto refill = [&]() {
+      const int jn = warp + (i + NSW) * NW;
+      if (jn < gm.n_stages) {
+        if (USE_TMA) fence_proxy_async_smem();
+        issue(jn, slot, next_page);
+        next_page = stage_page(jn + NW);
+      }
+      if (!USE_TMA) cp_async_commit();
+    };
+    uint32_t kf[EARLY ? KSTEPS : 1][4], vf[EARLY ? KSTEPS : 1][4];
+    if (EARLY) {
 #pragma unroll
-    for (int jj = 0; jj < NT; ++jj)
+      for (int kk = 0; kk < KSTEPS; ++kk) ldsm_x4(kf[kk], kbase + swz(krow, kk * 2 + (lane >> 4)));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sh[jj][e] = sl[jj][e] = 0.f;
-    {
-      const int row = ((lane >> 3) & 1) * 8 + (lane & 7);
+      for (int mt = 0; mt < KSTEPS; ++mt) ldsm_x4_trans(vf[mt], vbase + swz(vtok, mt * 2 + ((lane >> 3) & 1)));
+      __syncwarp();  // every lane's shared-memory reads of the slot are done
+      refill();
+    }
+
+    // ---- S^T = K . Q^T: hi and lo halves, even and odd k-steps in separate accumulators ----
+    float sacc[4][NT][4];
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        const int chunk = kk * 2 + (lane >> 4);
-        uint32_t a[4];
-        ldsm_x4(a, kbase + swz(row, chunk));
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int jj = 0; jj < NT; ++jj) {
-          TC<T>::mma(sh[jj], a, qh[kk][jj][0], qh[kk][jj][1]);
-          TC<T>::mma(sl[jj], a, ql[kk][jj][0], ql[kk][jj][1]);
-        }
+      for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[a][jj][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      uint32_t a[4];
+      if (EARLY) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = kf[kk][e];
+      } else {
+        ldsm_x4(a, kbase + swz(krow, kk * 2 + (lane >> 4)));
+      }
+#pragma unroll
+      for (int jj = 0; jj < NT; ++jj) {
+        TC<T>::mma(sacc[kk & 1][jj], a, qh[kk][jj][0], qh[kk][jj][1]);
+        TC<T>::mma(sacc[2 + (kk & 1)][jj], a, ql[kk][jj][0], ql[kk][jj][1]);
       }
     }
 
@@ -351,10 +392,13 @@ __global__ void __launch_bounds__(NW * 32)
     float pr[NT][4];
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {
-      float s0 = v0 ? sh[jj][0] + sl[jj][0] : -INFINITY;
-      float s1 = v0 ? sh[jj][1] + sl[jj][1] : -INFINITY;
-      float s2 = v1 ? sh[jj][2] + sl[jj][2] : -INFINITY;
-      float s3 = v1 ? sh[jj][3] + sl[jj][3] : -INFINITY;
+      float sv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv[e] = (sacc[0][jj][e] + sacc[1][jj][e]) + (sacc[2][jj][e] + sacc[3][jj][e]);
+      const float s0 = v0 ? sv[0] : -INFINITY;
+      const float s1 = v0 ? sv[1] : -INFINITY;
+      const float s2 = v1 ? sv[2] : -INFINITY;
+      const float s3 = v1 ? sv[3] : -INFINITY;
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -391,16 +435,6 @@ __global__ void __launch_bounds__(NW * 32)
         pt_lo[hh * 16 + tok] = TC<T>::bits(pr[jj][e] - hi);
       }
     }
-
-    // rows of the V tile outside [lo, hi) may hold stale or non-finite data: zero them
-    if (sg.lo > 0 || sg.hi < kStageRows) {
-      for (int idx = lane; idx < kStageRows * CPR; idx += 32) {
-        const int row = idx / CPR;
-        if (row < sg.lo || row >= sg.hi)
-          *reinterpret_cast<uint4*>(vt + (idx % CPR >> 3) * 2048 + row * 128 + (idx % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
     __syncwarp();
 
     // ---- O^T += V^T . P^T ----
@@ -417,30 +451,23 @@ __global__ void __launch_bounds__(NW * 32)
       bpl[jj][0] = b[2];
       bpl[jj][1] = b[3];
     }
-    {
-      const int tok = (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
-      for (int mt = 0; mt < KSTEPS; ++mt) {
-        const int chunk = mt * 2 + ((lane >> 3) & 1);
-        uint32_t a[4];
-        ldsm_x4_trans(a, vbase + swz(tok, chunk));
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      uint32_t a[4];
+      if (EARLY) {
 #pragma unroll
-        for (int jj = 0; jj < NT; ++jj) {
-          TC<T>::mma(o[mt][jj], a, bph[jj][0], bph[jj][1]);
-          TC<T>::mma(o[mt][jj], a, bpl[jj][0], bpl[jj][1]);
-        }
+        for (int e = 0; e < 4; ++e) a[e] = vf[mt][e];
+      } else {
+        ldsm_x4_trans(a, vbase + swz(vtok, mt * 2 + ((lane >> 3) & 1)));
+      }
+#pragma unroll
+      for (int jj = 0; jj < NT; ++jj) {
+        TC<T>::mma(o[mt][jj], a, bph[jj][0], bph[jj][1]);
+        TC<T>::mma(o[mt][jj], a, bpl[jj][0], bpl[jj][1]);
       }
     }
-    __syncwarp();
-
-    // ---- refill this slot with the warp's stage NSW rounds ahead ----
-    const int jn = warp + (i + NSW) * NW;
-    if (jn < gm.n_stages) {
-      if (USE_TMA) fence_proxy_async_smem();
-      issue(jn, slot, next_page);
-      next_page = stage_page(jn + NW);
-    }
-    if (!USE_TMA) cp_async_commit();
+    __syncwarp();  // the P^T buffer is rewritten by the next stage
+    if (!EARLY) refill();
   }
 
   if (USE_TMA) {

@@ -139,6 +139,8 @@ pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len, const 
   out->workspace_v_bytes = n * num_qo_heads * static_cast<int64_t>(head_dim) * 4;
   out->workspace_lse_bytes = n * num_qo_heads * 4;
   out->counter_bytes = static_cast<int64_t>(batch) * per_chunk * 4;
+  out->stack_members = 1;
+  out->out_row_step = 1;
   out->geometry_hash = geometry_hash(indptr, batch);
   if (n > cap_chunks) return PA_ECAPACITY;
 

@@ -30,6 +30,7 @@ KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF
 # Exported symbols of the C ABI (the header's declarations).
 ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
+               "pa_v2_cascade_detect", "pa_v2_cascade_split",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -46,7 +47,7 @@ class PlanStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "kv_dtype", "q_heads_per_cta",
         "q_groups", "pages_per_chunk", "lo_pages_per_chunk", "hi_pages_per_chunk", "num_chunks",
-        "needs_merge", "target_ctas", "total_ctas", "kernel")] + [
+        "needs_merge", "target_ctas", "total_ctas", "kernel", "stack_members", "out_row_step")] + [
         ("num_indices", ctypes.c_int64), ("workspace_v_bytes", ctypes.c_int64),
         ("workspace_lse_bytes", ctypes.c_int64), ("counter_bytes", ctypes.c_int64),
         ("geometry_hash", ctypes.c_uint64)]
@@ -74,7 +75,11 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_plan_matches.restype = i32
         L.pa_v2_decode_partial.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, f32, P, P, P, P]
         L.pa_v2_decode_partial.restype = i32
-        L.pa_v2_decode.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P, P, P, P]
+        L.pa_v2_decode.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P, P, P, P, P, P]
+        L.pa_v2_cascade_detect.argtypes = [P, P, P, i32, i32, i32, P, P, P]
+        L.pa_v2_cascade_detect.restype = i32
+        L.pa_v2_cascade_split.argtypes = [P, P, P, P, i32, P, i32, P, P, P, P, P, P, P, P]
+        L.pa_v2_cascade_split.restype = i32
         L.pa_v2_decode.restype = i32
         L.pa_v2_decode_noalloc.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P]
         L.pa_v2_decode_noalloc.restype = i32
@@ -197,6 +202,20 @@ def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None) -> int | None:
     return t.data_ptr()
 
 
+def _out_ptr(t: torch.Tensor, name: str, s: PlanStruct, per_row: int) -> int:
+    """Pointer of a final-output tensor whose rows may be `out_row_step` rows apart: either contiguous,
+    or a view whose leading dimension has stride out_row_step * per_row elements (rows interleaved with
+    another decode's rows for one pa_merge_states)."""
+    if not t.is_cuda or t.dtype != torch.float32:
+        raise ValueError(f"{name} must be a float32 CUDA tensor")
+    if t.is_contiguous():
+        return t.data_ptr()
+    inner = t[0] if t.dim() > 1 else t
+    if t.dim() < 2 or not inner.is_contiguous() or t.stride(0) != s.out_row_step * per_row:
+        raise ValueError(f"{name} must be contiguous, or rows {s.out_row_step} x {per_row} elements apart")
+    return t.data_ptr()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -254,7 +273,7 @@ def pa_merge_states(v_in, lse2_in, o_indptr, num_rows_out: int, v_out=None, lse2
 
 def pa_v2_decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
                  sm_scale: float, out=None, lse2_out=None, workspace=None, counters=None, status=None, stream=None,
-                 request_indices=None, kv_tile_indices=None, o_indptr=None):
+                 request_indices=None, kv_tile_indices=None, o_indptr=None, member_rows=None, out_rows=None):
     """One-launch decode (pa_v2_decode): partial kernel with the merge fused in.
 
     Returns (out [B, Hq, D] f32, lse2 [B, Hq] f32).  `workspace` = (v, lse) partial buffers sized by the
@@ -273,10 +292,13 @@ def pa_v2_decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, 
         wv = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
     if wl is None:
         wl = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    rows = s.batch * s.stack_members        # requests, or members of a stacked (cascade level 0) plan
+    heads = s.num_qo_heads // s.stack_members
     if out is None:
-        out = torch.empty(max(s.batch, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+        out = torch.empty(max(rows, 1) * s.out_row_step, heads, s.head_dim, device=dev,
+                          dtype=torch.float32)[::s.out_row_step]
     if lse2_out is None:
-        lse2_out = torch.empty(max(s.batch, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+        lse2_out = torch.empty(max(rows, 1) * s.out_row_step, heads, device=dev, dtype=torch.float32)[::s.out_row_step]
     if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
         raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
     if counters.numel() * 4 < s.counter_bytes:
@@ -289,11 +311,52 @@ def pa_v2_decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, 
         _dev_ptr(ri, "request_indices", torch.int32), _dev_ptr(ti, "kv_tile_indices", torch.int32),
         _dev_ptr(oi, "o_indptr", torch.int32), float(sm_scale), _dev_ptr(wv, "workspace_v", torch.float32),
         _dev_ptr(wl, "workspace_lse", torch.float32), _dev_ptr(counters, "counters", torch.int32),
-        _dev_ptr(out, "out", torch.float32), _dev_ptr(lse2_out, "lse2_out", torch.float32),
+        _out_ptr(out, "out", s, heads * s.head_dim) if out_rows is None else _dev_ptr(out, "out", torch.float32),
+        _out_ptr(lse2_out, "lse2_out", s, heads) if out_rows is None else _dev_ptr(lse2_out, "lse2_out", torch.float32),
+        _dev_ptr(member_rows, "member_rows", torch.int32), _dev_ptr(out_rows, "out_rows", torch.int32),
         _dev_ptr(status, "status", torch.int32), _stream(stream))
     if rc != PA_OK:
         raise PaError(rc, "pa_v2_decode")
-    return out[:s.batch], lse2_out[:s.batch]
+    return (out[:rows], lse2_out[:rows]) if out_rows is None else (out, lse2_out)
+
+
+def pa_v2_cascade_detect(indptr, indices, first_page_offset, min_shared_pages: int = 16, min_members: int = 2):
+    """Shared-prefix detection (pa_v2_cascade_detect); host arrays.  Returns (member flags [B], shared pages)."""
+    ip, idx, fp = _host_i32(indptr), _host_i32(indices), _host_i32(first_page_offset)
+    B = fp.numel()
+    flags = torch.zeros(max(B, 1), dtype=torch.int32)
+    nm, sh = ctypes.c_int32(), ctypes.c_int32()
+    rc = lib().pa_v2_cascade_detect(ip.data_ptr(), idx.data_ptr() if idx.numel() else None, fp.data_ptr(), B,
+                                    min_shared_pages, min_members, flags.data_ptr(), ctypes.byref(nm),
+                                    ctypes.byref(sh))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_cascade_detect")
+    return flags[:B], int(sh.value)
+
+
+def pa_v2_cascade_split(indptr, indices, last_page_len, first_page_offset, member_of, shared_pages: int):
+    """Level-1 table and row maps of a cascade batch (pa_v2_cascade_split); host arrays in and out."""
+    ip, idx, lp, fp, mo = (_host_i32(x) for x in (indptr, indices, last_page_len, first_page_offset, member_of))
+    B = lp.numel()
+    M = int(mo.sum())
+    l1_ip = torch.zeros(B + 1, dtype=torch.int32)
+    l1_idx = torch.zeros(max(1, idx.numel() - M * shared_pages), dtype=torch.int32)
+    l1_lp = torch.zeros(max(B, 1), dtype=torch.int32)
+    l1_fp = torch.zeros(max(B, 1), dtype=torch.int32)
+    mrows = torch.zeros(max(M, 1), dtype=torch.int32)
+    l0_rows = torch.zeros(max(M, 1), dtype=torch.int32)
+    l1_rows = torch.zeros(max(B, 1), dtype=torch.int32)
+    m_ip = torch.zeros(B + 1, dtype=torch.int32)
+    rc = lib().pa_v2_cascade_split(ip.data_ptr(), idx.data_ptr(), lp.data_ptr(), fp.data_ptr(), B, mo.data_ptr(),
+                                   shared_pages, l1_ip.data_ptr(), l1_idx.data_ptr(), l1_lp.data_ptr(),
+                                   l1_fp.data_ptr(), mrows.data_ptr(), l0_rows.data_ptr(), l1_rows.data_ptr(),
+                                   m_ip.data_ptr())
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_cascade_split")
+    n1 = int(l1_ip[-1])
+    return {"l1_indptr": l1_ip, "l1_indices": l1_idx[:n1], "l1_last_page_len": l1_lp[:B],
+            "l1_first_page_offset": l1_fp[:B], "member_rows": mrows[:M], "l0_out_rows": l0_rows[:M],
+            "l1_out_rows": l1_rows[:B], "merge_indptr": m_ip}
 
 
 def pa_v2_decode_noalloc(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,

@@ -248,6 +248,54 @@ def cascade_shared_prefix(seed: int = 1004, members: int = 4, prefix_tokens: int
                         suffix_last_page_len=lpl, suffix_lens=suffix_lens)
 
 
+def cascade_mixed_batch(seed: int = 1005, prefix_tokens: int = 2048, num_qo_heads: int = 16, num_kv_heads: int = 4,
+                        head_dim: int = 128, page_size: int = 16, dtype: torch.dtype = torch.float16) -> PagedBatch:
+    """A flat batch in which some requests share a whole-page prefix and others do not.
+
+    Requests 0, 2 and 5 share the first prefix_tokens / page_size page ids and then have private
+    suffixes; request 3 holds the same pages but its window starts mid-page (first_page_offset 5);
+    requests 1 and 4 share nothing."""
+    gen = torch.Generator().manual_seed(seed)
+    npre = prefix_tokens // page_size
+    kinds = ["member", "other", "member", "midpage", "other", "member"]
+    lens = [int(torch.randint(100, 1500, (1,), generator=gen)) for _ in kinds]
+    P = 4 * (npre + sum(-(-(L + 16) // page_size) for L in lens) + 8)
+    ids = torch.randperm(P, generator=gen).to(torch.int32)
+    prefix = ids[:npre]
+    nxt = npre
+    tables, fpos, seq = [], [], []
+    for kind, L in zip(kinds, lens):
+        if kind == "other":
+            pg, lpl = page_geometry(L, 0, page_size)
+            tables.append(ids[nxt:nxt + pg])
+            nxt += pg
+            fpos.append(0)
+            seq.append(L)
+        else:
+            f = 5 if kind == "midpage" else 0
+            total = prefix_tokens - f + L
+            pg, lpl = page_geometry(total, f, page_size)
+            own = pg - npre
+            tables.append(torch.cat([prefix, ids[nxt:nxt + own]]))
+            nxt += own
+            fpos.append(f)
+            seq.append(total)
+    indptr = [0]
+    for t in tables:
+        indptr.append(indptr[-1] + len(t))
+    geo = [page_geometry(L, f, page_size) for L, f in zip(seq, fpos)]
+    q = torch.randn(len(kinds), num_qo_heads, head_dim, generator=gen, dtype=torch.float32)
+    k_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    v_pool = _randn(gen, (P, page_size, num_kv_heads, head_dim), dtype)
+    return PagedBatch(
+        name="cascade_mixed_batch", q=q, k_pool=k_pool, v_pool=v_pool, indices=torch.cat(tables),
+        indptr=torch.tensor(indptr, dtype=torch.int32),
+        last_page_len=torch.tensor([l for _, l in geo], dtype=torch.int32),
+        first_page_offset=torch.tensor(fpos, dtype=torch.int32), seq_lens=seq, page_size=page_size,
+        num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim, scale=1.0 / math.sqrt(head_dim),
+        meta={"members": [0, 2, 5], "shared_pages": npre})
+
+
 def scatter_dense(name: str, dense_k: Sequence[torch.Tensor], dense_v: Sequence[torch.Tensor],
                   first_page_offsets: Sequence[int], page_size: int, num_qo_heads: int,
                   seed: int, slack: float = 2.0, order: str = "shuffled",

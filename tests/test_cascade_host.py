@@ -1,0 +1,94 @@
+"""Cascade detection and level split on the host (no GPU): the library against the oracle's rule."""
+import random
+
+import torch
+
+import oracle
+from paged_attention_decode_gb300 import pa_v2 as pa
+
+
+def _batch(rng, B, shared_groups):
+    """Random page tables where some requests copy a leading run of pages from a donor."""
+    tables, fpos = [], []
+    next_id = 0
+    for r in range(B):
+        n = rng.randint(1, 60)
+        pages = list(range(next_id, next_id + n))
+        next_id += n
+        if tables and rng.random() < shared_groups:
+            donor = rng.choice(tables)
+            k = rng.randint(1, len(donor))
+            pages = donor[:k] + pages[:max(1, n - k)]
+        tables.append(pages)
+        fpos.append(rng.choice([0, 0, 0, rng.randint(1, 15)]))
+    indptr = [0]
+    for t in tables:
+        indptr.append(indptr[-1] + len(t))
+    indices = [p for t in tables for p in t]
+    lpl = [rng.randint(max(1, f + 1) if len(t) == 1 else 1, 16) for t, f in zip(tables, fpos)]
+    return indptr, indices, lpl, fpos
+
+
+def test_detect_matches_the_oracle_rule_random():
+    rng = random.Random(5)
+    hits = 0
+    for case in range(400):
+        B = rng.randint(1, 12)
+        indptr, indices, lpl, fpo = _batch(rng, B, 0.6)
+        ms, mm = rng.choice([(1, 2), (4, 2), (16, 2), (3, 3)])
+        ref_members, ref_shared = oracle.cascade_detect_ref(indptr, indices, fpo, ms, mm)
+        flags, shared = pa.pa_v2_cascade_detect(indptr, indices, fpo, ms, mm)
+        got = [r for r in range(B) if int(flags[r])]
+        assert (got, shared) == (ref_members, ref_shared), (case, got, shared, ref_members, ref_shared)
+        hits += bool(got)
+    assert hits > 50
+
+
+def test_detect_rules_by_hand():
+    # three requests share pages 10..29; request 3 shares them too but starts mid-page; request 4 shares
+    # only page 10 and 11
+    t = [list(range(10, 30)) + [100 + i for i in range(5)],
+         list(range(10, 30)) + [200],
+         list(range(10, 30)) + [300, 301],
+         list(range(10, 30)) + [400],
+         [10, 11, 500]]
+    fpo = [0, 0, 0, 3, 0]
+    indptr = [0]
+    for x in t:
+        indptr.append(indptr[-1] + len(x))
+    indices = [p for x in t for p in x]
+    # the group keyed by page 10 is {0, 1, 2, 4}; request 4 caps the span at 2 pages
+    assert oracle.cascade_detect_ref(indptr, indices, fpo, 1, 2) == ([0, 1, 2, 4], 2)
+    flags, shared = pa.pa_v2_cascade_detect(indptr, indices, fpo, 1, 2)
+    assert flags.tolist() == [1, 1, 1, 0, 1] and shared == 2
+    # below the minimum span nothing qualifies
+    assert pa.pa_v2_cascade_detect(indptr, indices, fpo, 16, 2)[1] == 0
+    # a request whose span reaches its last page caps the span at pages - 1
+    t2 = [list(range(10, 30)), list(range(10, 30)) + [7]]
+    ip2 = [0, 20, 41]
+    idx2 = t2[0] + t2[1]
+    assert oracle.cascade_detect_ref(ip2, idx2, [0, 0], 1, 2) == ([0, 1], 19)
+    assert pa.pa_v2_cascade_detect(ip2, idx2, [0, 0], 1, 2)[1] == 19
+
+
+def test_split_rebuilds_the_flat_tables():
+    rng = random.Random(9)
+    for case in range(100):
+        B = rng.randint(2, 10)
+        indptr, indices, lpl, fpo = _batch(rng, B, 0.8)
+        flags, shared = pa.pa_v2_cascade_detect(indptr, indices, fpo, 1, 2)
+        if shared == 0:
+            continue
+        sp = pa.pa_v2_cascade_split(indptr, indices, lpl, fpo, flags, shared)
+        members = [r for r in range(B) if int(flags[r])]
+        assert sp["member_rows"].tolist() == members
+        first = members[0]
+        prefix = indices[indptr[first]:indptr[first] + shared]
+        mi = sp["merge_indptr"].tolist()
+        for r in range(B):
+            l1 = sp["l1_indices"][sp["l1_indptr"][r]:sp["l1_indptr"][r + 1]].tolist()
+            full = indices[indptr[r]:indptr[r + 1]]
+            assert (prefix + l1 if flags[r] else l1) == full
+            assert mi[r + 1] - mi[r] == (2 if flags[r] else 1)
+            assert sp["l1_out_rows"][r] == mi[r + 1] - 1
+        assert sp["l0_out_rows"].tolist() == [mi[r] for r in members]

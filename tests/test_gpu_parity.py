@@ -76,6 +76,77 @@ def test_cascade_flat_and_two_level():
     assert float((co - flat_o).abs().max()) <= 2 * OUT_TOL
 
 
+def test_cascade_driver_three_launches():
+    """The library's cascade path (stacked level 0 read in place, rows interleaved for one merge)."""
+    from paged_attention_decode_gb300 import cascade as C
+    cb = W.cascade_shared_prefix()
+    f = cb.flat
+    dt = pa.KV_DTYPES[f.dtype]
+    M, Hq, D = f.q.shape
+    t0 = pa.pa_v2_default_target_ctas(M * Hq, f.num_kv_heads, D, f.page_size, dt)
+    t1 = pa.pa_v2_default_target_ctas(Hq, f.num_kv_heads, D, f.page_size, dt)
+    fp1 = torch.zeros(M, dtype=torch.int32)
+    cp = C.cascade_plan(len(cb.prefix_indices), cb.suffix_indptr, cb.suffix_last_page_len, fp1, f.page_size, Hq,
+                        f.num_kv_heads, D, dt, t0, t1, cb.suffix_lens)
+    dev = "cuda"
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = (f.q.to(dev), f.k_pool.to(dev), f.v_pool.to(dev), cb.prefix_indices.to(dev), cb.suffix_indices.to(dev),
+            cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev), fp1.to(dev), f.scale)
+    out, lse = C.cascade_decode(cp, *args, status=status)
+    out2, lse2 = C.cascade_decode(cp, *args, status=status)   # twice: counters and buffers reused
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.cascade_ref(f.q, f.k_pool, f.v_pool, cb.prefix_indices, cb.suffix_indices,
+                                      cb.suffix_indptr, cb.suffix_last_page_len, f.scale)
+    assert_close(out, lse, ref_o, ref_l, "cascade driver")
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_cascade_on_a_mixed_batch():
+    """Detection + split + three launches on a batch with members, a mid-page sharer and strangers."""
+    from paged_attention_decode_gb300 import cascade as C
+    b = W.cascade_mixed_batch()
+    dt = pa.KV_DTYPES[b.dtype]
+    cp = C.plan_batch(b.indptr, b.indices, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
+                      b.num_kv_heads, b.head_dim, dt)
+    assert cp is not None and cp.members == 3 and cp.shared_pages == b.meta["shared_pages"]
+    d = b.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = C.decode_batch(cp, d.q, d.k_pool, d.v_pool, b.scale, status=status)
+    out2, lse2 = C.decode_batch(cp, d.q, d.k_pool, d.v_pool, b.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                    b.first_page_offset, b.scale)
+    assert_close(out, lse, ref_o, ref_l, "mixed-batch cascade")
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("M,G", [(2, 4), (4, 4), (3, 2)])
+def test_stacked_level0_reads_member_layout(M, G):
+    """stack_members: one request over shared pages serves M members' heads, read and written in member
+    layout; compared with the oracle on each member's own copy of the table."""
+    Hkv, D, ps, npre = 2, 128, 16, 37
+    g = torch.Generator().manual_seed(M * 10 + G)
+    P = 2 * npre
+    ids = torch.randperm(P, generator=g)[:npre].to(torch.int32)
+    q = torch.randn(M, Hkv * G, D, generator=g)
+    kp = torch.randn(P, ps, Hkv, D, generator=g).half()
+    vp = torch.randn(P, ps, Hkv, D, generator=g).half()
+    plan = pa.pa_v2_plan([0, npre], [ps], [0], ps, M * Hkv * G, Hkv, D, pa.PA_F16, 40)
+    plan.struct.stack_members = M
+    dev = "cuda"
+    out, lse = pa.pa_v2_decode(plan, q.to(dev), kp.to(dev), vp.to(dev), ids.to(dev),
+                               torch.tensor([0, npre], dtype=torch.int32, device=dev),
+                               torch.tensor([ps], dtype=torch.int32, device=dev),
+                               torch.zeros(1, dtype=torch.int32, device=dev), D ** -0.5)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attention(q, kp, vp, ids.repeat(M), torch.arange(0, (M + 1) * npre, npre, dtype=torch.int32),
+                                    [ps] * M, [0] * M, D ** -0.5)
+    assert out.shape == (M, Hkv * G, D)
+    assert_close(out, lse, ref_o, ref_l, "stacked level 0")
+
+
 def cascade_gpu(cb):
     """Level 0 over the shared pages with stacked heads, level 1 over the suffixes, one merge."""
     f = cb.flat

@@ -75,7 +75,7 @@ def test_exactly_full_final_page_is_page_size_not_zero():
 
 
 def test_geometry_identity_on_workloads():
-    for b in (W.tiny_csr(), W.sliding_window_batch(),
+    for b in (W.tiny_csr(), W.sliding_window_batch(), W.cascade_mixed_batch(),
               W.sparse_token_exact(cap=4096, selected=64, heads=2),
               W.cascade_shared_prefix(prefix_tokens=256, suffix_range=(3, 40)).flat):
         assert oracle.validate_geometry(b.indptr, b.last_page_len, b.first_page_offset, b.page_size,
@@ -391,6 +391,12 @@ def test_merge_of_disjoint_ranges_is_the_whole_range():
 # ---------------------------------------------------------------------------
 # cascade
 # ---------------------------------------------------------------------------
+
+def test_mixed_batch_detection_finds_the_planted_group():
+    b = W.cascade_mixed_batch()
+    assert oracle.cascade_detect_ref(b.indptr, b.indices, b.first_page_offset) == \
+        (b.meta["members"], b.meta["shared_pages"])
+
 
 def test_cascade_equals_flat_and_member_major_is_wrong():
     cb = W.cascade_shared_prefix(prefix_tokens=128, suffix_range=(5, 40), num_qo_heads=8, num_kv_heads=2,
