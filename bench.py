@@ -40,6 +40,8 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 METRIC = "decode KV-read GB/s (% of GB300 HBM peak) and µs/step at 32K context"
+STEP_TWO = "pa_v2_decode_partial + pa_merge_states (merge launched as a programmatic dependent)"
+STEP_FUSED = "pa_v2_decode (merge fused into the partial kernel)"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -63,8 +65,9 @@ def parse_args():
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
     ap.add_argument("--tune", action="store_true",
                     help="--workload runs: also time the chunk size picked by the autotuner")
-    ap.add_argument("--two-launch", action="store_true",
-                    help="time pa_v2_decode_partial + pa_merge_states instead of the one-launch pa_v2_decode")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the one-launch pa_v2_decode (merge fused into the partial kernel) instead of "
+                         "pa_v2_decode_partial + pa_merge_states")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
     ap.add_argument("--profile", type=int, default=0,
                     help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
@@ -330,8 +333,8 @@ def run_ours(args):
         pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len, d.first_page_offset,
                         b0.scale, out, lse, (wv, wl), counters, None, stream, ri, ti, oi)
 
-    step = step_two_launch if args.two_launch else step_fused
-    launches_per_step = 1 + int(plan.needs_merge) if args.two_launch else 1
+    step = step_fused if args.fused else step_two_launch
+    launches_per_step = 1 if args.fused else 1 + int(plan.needs_merge)
 
     if args.profile:
         with torch.cuda.stream(stream):
@@ -348,7 +351,7 @@ def run_ours(args):
     stream.synchronize()
     import oracle
     ref_o, ref_l = oracle.attention(*oracle_sample(b0, args.context))
-    o_now = (out if (plan.needs_merge or not args.two_launch) else wv[:B]).cpu().double().numpy()
+    o_now = (out if (plan.needs_merge or args.fused) else wv[:B]).cpu().double().numpy()
     err = float(abs(o_now - ref_o).max())
     if err > 2e-3:
         raise SystemExit(f"bench: GPU output disagrees with the oracle (max|d| = {err:.3e}); refusing to time")
@@ -445,6 +448,7 @@ def run_ours(args):
                    "head_dim": D, "page_size": b0.page_size, "context": args.context, "kv_dtype": "f16",
                    "kv_bytes_per_step": kv_bytes, "target_ctas": target, "pages_per_chunk": plan.pages_per_chunk,
                    "num_chunks": N, "ctas": plan.total_ctas, "merge": bool(plan.needs_merge),
+                   "step": STEP_FUSED if args.fused else STEP_TWO,
                    "l2": f"rotating {len(sets)} independent input sets ({len(sets) * kv_bytes >> 20} MiB of K/V "
                          "between reuses of a set; L2 is 126 MB)",
                    "cuda_graph": bool(graph is not None), "parallelism": f"replicas x{world}"},
@@ -467,7 +471,8 @@ def run_ours(args):
 
 def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     """Per step: one pinned H2D copy of q and the page table, the cached plan checked with
-    pa_v2_plan_matches, pa_v2_decode, one D2H copy of out + lse, stream sync."""
+    pa_v2_plan_matches, the decode launches (the same step as the device-timed region), one D2H copy of
+    out + lse, stream sync."""
     B, Hq, D = b0.batch, b0.num_qo_heads, b0.head_dim
     # one pinned staging buffer per input set: [q (f32) | indices | indptr | lpl | fpo] as 32-bit words
     host_in, views = [], []
@@ -503,8 +508,15 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
             o += B + 1
             lp = dev_in[o:o + B]
             fp = dev_in[o + B:o + 2 * B]
-            pa.pa_v2_decode(plan, q, sets[i % len(sets)].k_pool, sets[i % len(sets)].v_pool, idx, ip, lp, fp,
-                            b0.scale, out, lse, (wv, wl), counters, None, stream, ri, ti, oi)
+            kp, vp = sets[i % len(sets)].k_pool, sets[i % len(sets)].v_pool
+            if args.fused:
+                pa.pa_v2_decode(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, out, lse, (wv, wl), counters, None,
+                                stream, ri, ti, oi)
+            elif plan.needs_merge:
+                pa.pa_v2_decode_partial(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, wv, wl, None, stream, ri, ti)
+                pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
+            else:
+                pa.pa_v2_decode_partial(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, out, lse, None, stream, ri, ti)
             res_h.copy_(res_d, non_blocking=True)
         stream.synchronize()
 
@@ -518,8 +530,8 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     kv_bytes = b0.kv_bytes()
     return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "per step: 1 pinned H2D (q + page table), pa_v2_plan_matches, pa_v2_decode, 1 D2H (out + lse), "
-                    "stream sync; ctypes binding"}
+            "path": "per step: 1 pinned H2D (q + page table), pa_v2_plan_matches, "
+                    + (STEP_FUSED if args.fused else STEP_TWO) + ", 1 D2H (out + lse), stream sync; ctypes binding"}
 
 
 def run_workload(args):

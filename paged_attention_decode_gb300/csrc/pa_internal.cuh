@@ -394,6 +394,26 @@ inline bool tc_uses_tma(int page_size) {
   return page_size % 8 == 0 && (page_size <= kStageRows || page_size % kStageRows == 0);
 }
 
+// Launch `fn` as a programmatic dependent of the kernel before it in the
+// stream: its CTAs may become resident while that kernel is finishing, and
+// each one waits (griddepcontrol.wait) for it to complete before its first
+// global-memory access.  Without a programmatic predecessor the wait is a no-op.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, static_cast<Args&&>(args)...);
+}
+
 // Shared-memory opt-in above 48 KB, once per kernel and device (safe to call
 // under stream capture after the first call).
 bool prepare_kernel(const void* fn, size_t smem);

@@ -12,11 +12,12 @@
 // exact identity (w = 1).
 //
 // Layout on sm_103a: the merge reads little data (the partial workspace) and
-// is bound by memory latency, so it is organised to keep many independent
-// loads in flight.  One CTA of 4 warps per (output row, head): the CTA takes
-// the group's max LSE in one round of loads, then each warp walks a quarter of
-// the group's rows with 128-bit loads (4 head-dim floats per lane) unrolled 8
-// deep, and the warps' sums meet in shared memory.
+// is bound by memory latency, so it is organised to need one round of loads
+// for up to 32 partial rows.  One CTA of 4 warps per (output row, head): warp w
+// loads the LSE and the 128-bit V slice (4 head-dim floats per lane) of rows
+// i0 + w, i0 + w + 4, ... eight at a time, keeps a running maximum and rescales
+// its sum when the maximum grows, and the four warps' (max, weight sum, V sum)
+// meet in shared memory, each scaled by 2^(its max - the group max).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -47,6 +48,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   __shared__ float wsum_s[kMergeWarps];
   __shared__ __align__(16) float acc_s[kMergeWarps][128];
 
+  // the kernel that follows (normally the next step's partial kernel) may be
+  // scheduled now; it waits for this grid to finish
+  pdl_launch_dependents();
   // launched as a programmatic dependent of the partial kernel: wait for its
   // grid to complete (and its writes to be visible) before reading anything
   pdl_wait_prerequisites();
@@ -63,30 +67,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
   const size_t hs = (size_t)num_heads;
 
-  // group max of the LSEs
-  float m = -INFINITY;
-  for (int i = i0 + threadIdx.x; i < i1; i += kMergeWarps * 32) m = fmaxf(m, lse_in[i * hs + h]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, red[w]);
-
   float* out = v_out + ((size_t)r * num_heads + h) * head_dim;
-  if (m == -INFINITY) {
-    for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) out[d] = 0.f;
-    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = -INFINITY;
-    return;
-  }
-
   if (VECTOR) {
     const int d4n = head_dim >> 2;
     const bool active = lane < d4n;
+    float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float ws = 0.f;
-    // warp w takes rows i0 + w, i0 + w + 4, ...; 8 independent row loads per round
     for (int base = i0 + warp; base < i1; base += kMergeWarps * kMergeUnroll) {
       float l[kMergeUnroll];
       float4 v[kMergeUnroll];
@@ -97,31 +83,71 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         v[u] = (i < i1 && active) ? reinterpret_cast<const float4*>(v_in + (i * hs + h) * head_dim)[lane]
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float mb = m;
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) mb = fmaxf(mb, l[u]);
+      if (mb == -INFINITY) continue;
+      const float sc = merge_weight(m, mb);  // 0 while nothing has been summed
+      ws *= sc;
+      acc.x *= sc;
+      acc.y *= sc;
+      acc.z *= sc;
+      acc.w *= sc;
 #pragma unroll
       for (int u = 0; u < kMergeUnroll; ++u) {
-        const float w = merge_weight(l[u], m);
+        const float w = merge_weight(l[u], mb);
         ws += w;
         acc.x = fmaf(w, v[u].x, acc.x);
         acc.y = fmaf(w, v[u].y, acc.y);
         acc.z = fmaf(w, v[u].z, acc.z);
         acc.w = fmaf(w, v[u].w, acc.w);
       }
+      m = mb;
     }
     if (active) reinterpret_cast<float4*>(acc_s[warp])[lane] = acc;
-    if (lane == 0) wsum_s[warp] = ws;
+    if (lane == 0) {
+      red[warp] = m;
+      wsum_s[warp] = ws;
+    }
     __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+    if (M == -INFINITY) {
+      for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) out[d] = 0.f;
+      if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = -INFINITY;
+      return;
+    }
+    float scw[kMergeWarps];
     float W = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) W += wsum_s[w];
+    for (int w = 0; w < kMergeWarps; ++w) {
+      scw[w] = merge_weight(red[w], M);
+      W = fmaf(wsum_s[w], scw[w], W);
+    }
     for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) {
       float a = 0.f;
 #pragma unroll
-      for (int w = 0; w < kMergeWarps; ++w) a += acc_s[w][d];
+      for (int w = 0; w < kMergeWarps; ++w) a = fmaf(acc_s[w][d], scw[w], a);
       out[d] = a / W;
     }
-    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = fast_log2(W) + m;
+    if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = fast_log2(W) + M;
   } else {
     // general head_dim: the whole CTA walks the rows, one head-dim element per thread
+    float m = -INFINITY;
+    for (int i = i0 + threadIdx.x; i < i1; i += kMergeWarps * 32) m = fmaxf(m, lse_in[i * hs + h]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, red[w]);
+    if (m == -INFINITY) {
+      for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) out[d] = 0.f;
+      if (threadIdx.x == 0) lse_out[(size_t)r * num_heads + h] = -INFINITY;
+      return;
+    }
     float W = 0.f;
     for (int i = i0; i < i1; ++i) W += merge_weight(lse_in[i * hs + h], m);
     for (int d = threadIdx.x; d < head_dim; d += kMergeWarps * 32) {

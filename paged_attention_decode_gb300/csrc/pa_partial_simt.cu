@@ -143,8 +143,13 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int nheads = min(p.hpc, p.group - qg * p.hpc);
   const int ps = p.page_size;
 
-  // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+  // the kernel that follows (the merge, or the next step) may be scheduled now;
+  // it waits for this grid to finish
   pdl_launch_dependents();
+
+  // launched as a programmatic dependent: the kernel before this one in the
+  // stream has completed, and its writes are visible, once this returns
+  pdl_wait_prerequisites();
 
   // ---- chunk geometry ----
   int r;
@@ -158,6 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     fence_barrier_init();
   }
   __syncwarp();
+
 
   T* mystages = stages + (size_t)warp * NSW * 2 * SIDE;
   const uint64_t policy = policy_evict_first();
@@ -412,8 +418,8 @@ int launch_partial_simt(const LaunchArgs& a) {
   if (!simt_pick(a.kv_dtype, a.head_dim, a.p.hpc, &inst)) return PA_EUNSUPPORTED;
   if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
   dim3 grid(a.num_chunks, a.p.num_kv_heads * a.p.q_groups);
-  inst.fn<<<grid, kWarps * 32, inst.smem, a.stream>>>(*a.tm_k, *a.tm_v, a.p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+  const cudaError_t rc = launch_dependent(inst.fn, grid, dim3(kWarps * 32), inst.smem, a.stream, *a.tm_k, *a.tm_v, a.p);
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
 int occupancy_partial_simt(int kv_dtype, int head_dim, int hpc, int* blocks_per_sm) {

@@ -169,8 +169,13 @@ __global__ void __launch_bounds__(NW * 32)
   const int nheads = min(p.hpc, p.group - qg * p.hpc);
   const int ps = p.page_size;
 
-  // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+  // the kernel that follows (the merge, or the next step) may be scheduled now;
+  // it waits for this grid to finish
   pdl_launch_dependents();
+
+  // launched as a programmatic dependent: the kernel before this one in the
+  // stream has completed, and its writes are visible, once this returns
+  pdl_wait_prerequisites();
 
   int r;
   const ChunkGeom gm = chunk_geom(p, c, &r);
@@ -562,8 +567,8 @@ int launch_partial_tc(const LaunchArgs& a, bool use_tma) {
   if (!tc_pick(a.kv_dtype, a.head_dim, a.p.hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
   if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
   dim3 grid(a.num_chunks, a.p.num_kv_heads * a.p.q_groups);
-  inst.fn<<<grid, kTcWarps * 32, inst.smem, a.stream>>>(*a.tm_k, *a.tm_v, a.p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+  const cudaError_t rc = launch_dependent(inst.fn, grid, dim3(kTcWarps * 32), inst.smem, a.stream, *a.tm_k, *a.tm_v, a.p);
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
 }
 
 int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int* blocks_per_sm) {

@@ -297,3 +297,52 @@ def test_merge_regrouping_is_associative_on_gpu():
     again, al = pa.pa_merge_states(part, pl, torch.tensor([0, 3], dtype=torch.int32, device="cuda"), 1)
     torch.cuda.synchronize()
     assert float((again - full).abs().max()) <= 1e-5 and float((al - fl).abs().max()) <= 1e-5
+
+
+# ---------------------------------------------------------------------------
+# device-side bounds checks: bad device data is recorded in the status word, not read
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ps", [16, 4])
+def test_out_of_range_page_id_is_reported_not_read(ps):
+    # page_size 16 stages with TMA (the box is redirected past the pool's end, which TMA
+    # zero-fills); page_size 4 stages with cp.async (the copy is skipped)
+    b = W.make_batch("badpage", [200, 90], [0, 3], ps, 8, 2, 128, torch.float16, seed=17)
+    plan = make_plan(b, target=64)
+    d = b.to("cuda")
+    bad = d.indices.clone()
+    bad[3] = b.num_pages
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, bad, d.indptr, d.last_page_len, d.first_page_offset, b.scale,
+                    status=status)
+    torch.cuda.synchronize()
+    word = int(status.item())
+    assert word & pa.DEVICE_BAD_PAGE and pa.pa_status_from_device(word) == pa.PA_EOOB
+    # every CTA still finished, so the ticket counters are back at zero and a clean call is exact
+    assert int(plan.device_counters("cuda").abs().sum()) == 0
+    check_batch(b, plan=plan, d=d)
+
+
+def test_bad_o_indptr_is_reported():
+    v = torch.randn(4, 2, 64, device="cuda")
+    l = torch.randn(4, 2, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_merge_states(v, l, torch.tensor([0, 3, 2], dtype=torch.int32, device="cuda"), 2, status=status)
+    pa.pa_merge_states(v, l, torch.tensor([0, 9], dtype=torch.int32, device="cuda"), 1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pa.DEVICE_BAD_INDPTR
+
+
+def test_out_of_range_request_index_is_reported():
+    b = W.make_batch("badreq", [300], [0], 16, 8, 2, 128, torch.float16, seed=18)
+    plan = make_plan(b, target=16)
+    d = b.to("cuda")
+    ri, ti, _ = plan.device_arrays("cuda")
+    bad_ri = ri.clone()
+    bad_ri[0] = 7
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                            d.first_page_offset, b.scale, status=status, request_indices=bad_ri,
+                            kv_tile_indices=ti)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pa.DEVICE_BAD_REQUEST
