@@ -536,9 +536,10 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
 
 def run_workload(args):
     """Per-step timing of one of the other workloads: every step starts with a cold L2 (a 512 MiB
-    buffer is read between steps, outside the event pair), the step is the one-launch pa_v2_decode
-    (the cascade: level 0 + level 1 + one pa_merge_states, against the flat pa_v2_decode of the same batch).
-    The buffer is read, not written, so no dirty lines are written back during the step."""
+    buffer is read between steps, outside the event pair).  Arms: "two" = pa_v2_decode_partial +
+    pa_merge_states (the default step, `value`), "fused" = the one-launch pa_v2_decode; the cascade adds
+    level 0 + level 1 + one pa_merge_states, against the flat arms of the same batch.  The buffer is
+    read, not written, so no dirty lines are written back during the step."""
     from paged_attention_decode_gb300 import build as pa_build
     from paged_attention_decode_gb300 import pa_v2 as pa
     from paged_attention_decode_gb300 import workloads as W
@@ -576,12 +577,22 @@ def run_workload(args):
                 torch.empty(max(1, pl.num_chunks), pl.num_qo_heads, device=dev))
 
     ws = workspace(plan)
+    o_indptr = plan.device_arrays(dev)[2]
 
     def flat_step():
         pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len, d.first_page_offset,
                         b.scale, out, lse, ws, None, None, stream)
 
-    steps = {"flat": (flat_step, b.kv_bytes())}
+    def two_step():
+        if plan.needs_merge:
+            pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                    d.first_page_offset, b.scale, ws[0], ws[1], None, stream)
+            pa.pa_merge_states(ws[0], ws[1], o_indptr, b.batch, out, lse, None, stream)
+        else:
+            pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                    d.first_page_offset, b.scale, out, lse, None, stream)
+
+    steps = {"two": (two_step, b.kv_bytes()), "fused": (flat_step, b.kv_bytes())}
     if cascade:
         from paged_attention_decode_gb300 import cascade as C
         M, Hq, D = b.q.shape
@@ -616,15 +627,21 @@ def run_workload(args):
     # correctness guard before timing
     ref_o, _ = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                 b.first_page_offset, b.scale)
-    with torch.cuda.stream(stream):
-        flat_step()
-        if cascade:
-            steps["cascade"][0]()
-    stream.synchronize()
-    for name, got in (("flat", out),) + ((("cascade", c_out),) if cascade else ()):
-        err = float(abs(got.cpu().double().numpy() - ref_o).max())
-        if err > 2e-3:
+    for name in ("two", "fused"):
+        out.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            steps[name][0]()
+        stream.synchronize()
+        err = float(abs(out.cpu().double().numpy() - ref_o).max())
+        if not err <= 2e-3:
             raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}); refusing to time")
+    if cascade:
+        with torch.cuda.stream(stream):
+            steps["cascade"][0]()
+        stream.synchronize()
+        err = float(abs(c_out.cpu().double().numpy() - ref_o).max())
+        if not err <= 2e-3:
+            raise SystemExit(f"bench: cascade output disagrees with the oracle ({err:.3e}); refusing to time")
 
     res = {}
     for name, (fn, nbytes) in steps.items():
@@ -644,7 +661,7 @@ def run_workload(args):
                      "us_p90": t[(9 * len(t)) // 10] * 1e3, "kv_bytes_per_step": nbytes,
                      "kv_read_gbs": nbytes / (med * 1e-3) / 1e9}
     peak, peak_kind = measured_peak()
-    main = res["cascade" if cascade else "flat"]
+    main = res["cascade" if cascade else "two"]
     line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main["us_per_step_median"],
             "unit": "us/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "dtype": "f32", "data": "synthetic",

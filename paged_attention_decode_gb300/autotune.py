@@ -13,9 +13,10 @@ largest size whose CTA count *reaches* the target, which can overshoot one
 wave by up to (requests x KV heads x q-groups - 1) CTAs and so run a nearly
 empty second wave; the wave-aligned sizes are the candidates that avoid it.
 
-Each candidate is timed as ``pa_v2_decode`` launches (partial kernel with the
-fused merge) on the caller's inputs, each launch after a read of a buffer
-larger than L2, CUDA events on the launching stream, median of `reps`.
+Each candidate is timed as a decode step on the caller's inputs -- by default
+``pa_v2_decode_partial`` then ``pa_merge_states`` (``fused=True``: the one-launch
+``pa_v2_decode``) -- each step after a read of a buffer larger than L2, CUDA
+events on the launching stream, median of `reps`.
 """
 from __future__ import annotations
 
@@ -70,8 +71,8 @@ def candidates(indptr, num_kv_heads: int, q_groups: int, wave_ctas: int, default
 
 
 def tune(batch, device=None, target_ctas: int | None = None, reps: int = 20, extra: list[int] | None = None,
-         stream=None) -> TuneResult:
-    """Time pa_v2_decode on `batch` (a workloads.PagedBatch, CPU or device) for each candidate chunk size."""
+         stream=None, fused: bool = False) -> TuneResult:
+    """Time a decode step on `batch` (a workloads.PagedBatch, CPU or device) for each candidate chunk size."""
     dev = torch.device(device or "cuda")
     d = batch.to(dev)
     dt = pa.KV_DTYPES[batch.dtype]
@@ -95,14 +96,23 @@ def tune(batch, device=None, target_ctas: int | None = None, reps: int = 20, ext
             batch.num_kv_heads, batch.head_dim, dt, target, ppc, batch.seq_lens)
         ws = (torch.empty(plan.num_chunks, plan.num_qo_heads, plan.head_dim, device=dev),
               torch.empty(plan.num_chunks, plan.num_qo_heads, device=dev))
+        oi = plan.device_arrays(dev)[2]
         evs = []
         with torch.cuda.stream(stream):
             for i in range(reps + 3):
                 flush.sum()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
-                                d.first_page_offset, batch.scale, out, lse, ws, None, None, stream)
+                if fused:
+                    pa.pa_v2_decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                    d.first_page_offset, batch.scale, out, lse, ws, None, None, stream)
+                elif plan.needs_merge:
+                    pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                            d.first_page_offset, batch.scale, ws[0], ws[1], None, stream)
+                    pa.pa_merge_states(ws[0], ws[1], oi, batch.batch, out, lse, None, stream)
+                else:
+                    pa.pa_v2_decode_partial(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                            d.first_page_offset, batch.scale, out, lse, None, stream)
                 e1.record(stream)
                 evs.append((e0, e1))
         stream.synchronize()

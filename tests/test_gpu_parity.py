@@ -346,3 +346,18 @@ def test_out_of_range_request_index_is_reported():
                             kv_tile_indices=ti)
     torch.cuda.synchronize()
     assert int(status.item()) & pa.DEVICE_BAD_REQUEST
+
+
+# ---------------------------------------------------------------------------
+# chunk-size autotuner: real timed launches, and the tuned plan is still exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_autotune_times_candidates_and_tuned_plan_is_exact(fused):
+    from paged_attention_decode_gb300 import autotune
+    b = W.make_batch("tune", [3000, 700, 1, 0], [0, 5, 0, 0], 16, 8, 2, 128, torch.float16, seed=19)
+    res = autotune.tune(b, "cuda", reps=3, fused=fused)
+    assert res.default_pages_per_chunk in res.times_us
+    assert res.pages_per_chunk in res.times_us
+    assert all(t > 0 for t in res.times_us.values())
+    check_batch(b, override=res.pages_per_chunk)
