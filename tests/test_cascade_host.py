@@ -92,3 +92,20 @@ def test_split_rebuilds_the_flat_tables():
             assert mi[r + 1] - mi[r] == (2 if flags[r] else 1)
             assert sp["l1_out_rows"][r] == mi[r + 1] - 1
         assert sp["l0_out_rows"].tolist() == [mi[r] for r in members]
+
+
+def test_split_wave_and_chunk_fit():
+    from paged_attention_decode_gb300 import cascade as C
+    # one wave of 152 split 2:1 by bytes; each level keeps at least one chunk's CTAs
+    assert C.split_wave(152, 2, 1, 8, 32) == (101, 51)
+    assert C.split_wave(152, 1000, 1, 8, 32) == (120, 32)
+    assert C.split_wave(152, 1, 1000, 8, 32) == (8, 144)
+    # smallest chunk size whose CTAs fit the budget, by brute force
+    rng = random.Random(3)
+    for _ in range(300):
+        pages = [rng.randint(0, 300) for _ in range(rng.randint(1, 6))]
+        per = rng.choice([1, 8, 16])
+        budget = rng.randint(1, 400)
+        ppc = C.fit_pages_per_chunk(pages, per, budget)
+        fits = [k for k in range(1, max(pages + [1]) + 1) if C._chunks(pages, k) * per <= budget]
+        assert ppc == (min(fits) if fits else max(pages + [1]))
