@@ -31,7 +31,12 @@
  *    OR-ing PA_DEVICE_* bits.  The status word is read by the caller after
  *    the stream has synchronized.
  *  - Streams.  Device calls are asynchronous on the given cudaStream_t
- *    (passed as void*; NULL is the legacy default stream).
+ *    (passed as void*; NULL is the legacy default stream).  Every kernel is
+ *    launched with programmatic stream serialization: it may become resident
+ *    while the kernel before it in the stream is finishing, but it waits for
+ *    that kernel to complete (griddepcontrol.wait) before its first
+ *    global-memory access, so stream order is kept for every buffer.  Each
+ *    kernel also lets the one after it be scheduled early, at its own start.
  *  - Units.  Every LSE is in log2 units (scores run in base 2 with log2(e)
  *    folded into the scale); the natural-log LSE is lse2 * ln 2.
  *  - Layouts are row-major and contiguous:
