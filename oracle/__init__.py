@@ -12,6 +12,13 @@ Cascade composition (``cascade_ref``) follows cascade-attention.md (issue
 stacked ``h0 = kv * (M * G) + m * G + g``, level 1 attends each member's
 private suffix, and one merge pairs each member's two states.
 ``cascade_detect_ref`` is that page's detection rule written as plain loops.
+
+Block-sparse selections (sparse-paged-decode.md, issue #904: the paragraphs on
+``selection_from_blocks`` and on the final block): ``selection_rows_ref``
+expands the selected block ids of each request into the token rows a
+token-exact (page_size 1) page table lists, and ``selection_pages_ref`` gives
+the block-granular (page_size = block size) page list of a pool-backed cache.
+Both are plain loops over integers.
 """
 from __future__ import annotations
 
@@ -161,6 +168,17 @@ def resolve_rows(indices, indptr, first_page_offset, page_size, r: int, n: int) 
     return [int(L.ora_resolve_row(_ptr(idx), _ptr(ip), _ptr(fp), page_size, r, i)) for i in range(n)]
 
 
+def _check_table(ip, lp, fp, idx, ps, num_pages, q_batch):
+    """Refuse a page table the C routines would read outside of (a test-side mistake, not a result)."""
+    if len(ip) != len(lp) + 1 or len(fp) != len(lp) or len(lp) != q_batch:
+        raise ValueError("page-table arrays disagree on the batch size")
+    if len(ip) and int(ip[-1]) > len(idx):
+        raise ValueError(f"indptr[-1] = {int(ip[-1])} exceeds the {len(idx)} indices given")
+    code = validate_geometry(ip, lp, fp, ps, idx, num_pages)
+    if code != GEOM_OK:
+        raise ValueError(f"page table breaks the geometry rules (code {code})")
+
+
 def attention(q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, scale):
     """Decode attention for every (request, query head): (out [B,Hq,D] f64, lse2 [B,Hq] f64)."""
     qf = _f32(q)
@@ -171,6 +189,7 @@ def attention(q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offs
     P, ps, Hkv, Dk = kp.shape
     assert Dk == D
     idx, ip, lp, fp = _i32(indices), _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    _check_table(ip, lp, fp, idx, ps, P, B)
     out = np.zeros((B, Hq, D), np.float64)
     lse = np.zeros((B, Hq), np.float64)
     lib().ora_attention(_ptr(qf), _ptr(kp), _ptr(vp), code, _ptr(idx), _ptr(ip), _ptr(lp), _ptr(fp),
@@ -187,6 +206,7 @@ def partials(q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offse
     vp, _ = _pool(v_pool)
     P, ps, Hkv, _ = kp.shape
     idx, ip, lp, fp = _i32(indices), _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    _check_table(ip, lp, fp, idx, ps, P, B)
     ri, ti = _i32(request_indices), _i32(kv_tile_indices)
     N = len(ri)
     out = np.zeros((N, Hq, D), np.float64)
@@ -313,3 +333,57 @@ def cascade_detect_ref(indptr, indices, first_page_offset, min_shared_pages: int
     if len(best) < max(2, min_members) or best_shared < min_shared_pages:
         return [], 0
     return list(best), best_shared
+
+
+def selection_rows_ref(block_ids, block_size: int, kv_len: int, request_stride: int):
+    """Token rows of a block-sparse selection (sparse-paged-decode.md: "selection_from_blocks expands
+    block ids into token rows"; the final-block paragraph: the final block is never scored and is
+    appended unconditionally, its live rows only).
+
+    block_ids: [R, topk] ints, each in [0, nb - 1) with nb = ceil(kv_len / block_size).  Request r's
+    rows, in this order: for each selected block j (as given), r * request_stride + j * block_size + e
+    for e in [0, block_size); then the final block's rows r * request_stride + (nb - 1) * block_size + e
+    for e in [0, kv_len - (nb - 1) * block_size).  Returns (indices int32 [R * per_request], per_request).
+    """
+    ids = [list(map(int, row)) for row in torch.as_tensor(block_ids).reshape(len(block_ids), -1).tolist()]
+    nb = (kv_len + block_size - 1) // block_size
+    last = kv_len - (nb - 1) * block_size
+    out = []
+    for r, sel in enumerate(ids):
+        base = r * request_stride
+        for j in sel:
+            if not 0 <= j < nb - 1:
+                raise ValueError(f"block id {j} of request {r} outside the scored range [0, {nb - 1})")
+            for e in range(block_size):
+                out.append(base + j * block_size + e)
+        for e in range(last):
+            out.append(base + (nb - 1) * block_size + e)
+    per_request = len(ids[0]) * block_size + last if ids else 0
+    return torch.tensor(out, dtype=torch.int32), per_request
+
+
+def sparse_csr_ref(num_requests: int, per_request: int):
+    """(indptr, last_page_len, first_page_offset) of a token-exact selection: every request lists
+    `per_request` one-token pages (sparse-paged-decode.md: the CSR structure follows from the request
+    count and the per-request count alone)."""
+    indptr = torch.tensor([r * per_request for r in range(num_requests + 1)], dtype=torch.int32)
+    ones = torch.tensor([1 if per_request else 0] * num_requests, dtype=torch.int32)
+    return indptr, ones, torch.zeros(num_requests, dtype=torch.int32)
+
+
+def selection_pages_ref(block_ids, block_size: int, kv_len: int, blocks_per_request: int):
+    """Block-granular page table of a pool-backed cache whose request r owns pool pages
+    [r * blocks_per_request, (r + 1) * blocks_per_request) (sparse-paged-decode.md: feed the selected
+    block ids through as indices with the pool's block size as page_size).  The final block goes last so
+    that last_page_len can carry its live length.  Returns (indices, indptr, last_page_len,
+    first_page_offset)."""
+    ids = [list(map(int, row)) for row in torch.as_tensor(block_ids).reshape(len(block_ids), -1).tolist()]
+    nb = (kv_len + block_size - 1) // block_size
+    last = kv_len - (nb - 1) * block_size
+    pages, indptr = [], [0]
+    for r, sel in enumerate(ids):
+        pages += [r * blocks_per_request + j for j in sel] + [r * blocks_per_request + nb - 1]
+        indptr.append(len(pages))
+    R = len(ids)
+    return (torch.tensor(pages, dtype=torch.int32), torch.tensor(indptr, dtype=torch.int32),
+            torch.full((R,), last, dtype=torch.int32), torch.zeros(R, dtype=torch.int32))
