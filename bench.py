@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--context", type=int, default=32768)
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix",
-                             "tiny_csr"],
+                             "tiny_csr", "block_sparse_selection"],
                     help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
                          "(cold L2 for every step)")
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
@@ -690,10 +690,127 @@ def run_workload(args):
     print(json.dumps(line), flush=True)
 
 
+def _time_cold(fn, stream, flush, warmup, steps, graph):
+    """Median, p10, p90 (us) of `fn` per step with a 512 MiB read before each step, replayed from a CUDA
+    graph of that step when `graph`."""
+    run = fn
+    if graph:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        run = g.replay
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(warmup + steps):
+            flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            times.append((e0, e1))
+    stream.synchronize()
+    t = sorted(a.elapsed_time(z) * 1e3 for a, z in times[warmup:])
+    return t[len(t) // 2], t[len(t) // 10], t[(9 * len(t)) // 10]
+
+
+def run_block_sparse(args):
+    """Block-sparse decode (sparse-paged-decode.md): MiniMax-M3 geometry, 16 selected blocks of 128 rows
+    plus the partial final block per request.  Arms: "token_exact" = pa_selection_from_blocks + the
+    page_size-1 decode (partial + merge), the expansion inside every step; "block_granular" = the same
+    selection as 128-row pages of a pool-backed view of the same allocation (page list built once)."""
+    from paged_attention_decode_gb300 import build as pa_build
+    from paged_attention_decode_gb300 import pa_v2 as pa
+    from paged_attention_decode_gb300 import workloads as W
+    import oracle
+
+    pa_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    s = W.block_sparse_selection()
+    d = s.to(dev)
+    R, n_rep, D = s.q.shape
+    C, topk = s.block_size, s.block_ids.shape[1]
+    dt = pa.KV_DTYPES[s.k_pool.dtype]
+    per = pa.pa_selection_rows_per_request(topk, C, s.kv_len)
+    ip, lp, fp = pa.pa_sparse_csr(R, per)
+    plan = pa.pa_v2_plan(ip, lp, fp, 1, n_rep, 1, D, dt, pa.pa_v2_default_target_ctas(n_rep, 1, D, 1, dt))
+    ipd, lpd, fpd = ip.to(dev), lp.to(dev), fp.to(dev)
+    rows = torch.empty(R * per, dtype=torch.int32, device=dev)
+    out = torch.empty(R, n_rep, D, device=dev)
+    lse = torch.empty(R, n_rep, device=dev)
+    ws = (torch.empty(max(1, plan.num_chunks), n_rep, D, device=dev),
+          torch.empty(max(1, plan.num_chunks), n_rep, device=dev))
+
+    def token_exact():
+        pa.pa_selection_from_blocks(d.block_ids, C, s.kv_len, s.cap, rows, None, stream)
+        pa.decode(plan, d.q, d.k_pool, d.v_pool, rows, ipd, lpd, fpd, s.scale, out, lse, ws, None, stream)
+
+    # block-granular page list of the pool view [R * cap / C, C, 1, D]: request r's selected blocks, then
+    # its final block (host marshalling of the selection, once)
+    bpr = s.cap // C
+    nb = -(-s.kv_len // C)
+    pages = torch.cat([torch.cat([r * bpr + s.block_ids[r], torch.tensor([r * bpr + nb - 1], dtype=torch.int32)])
+                       for r in range(R)]).to(torch.int32)
+    ip2 = torch.arange(0, (R + 1) * (topk + 1), topk + 1, dtype=torch.int32)
+    lp2 = torch.full((R,), s.kv_len - (nb - 1) * C, dtype=torch.int32)
+    fp2 = torch.zeros(R, dtype=torch.int32)
+    plan2 = pa.pa_v2_plan(ip2, lp2, fp2, C, n_rep, 1, D, dt, pa.pa_v2_default_target_ctas(n_rep, 1, D, C, dt))
+    kp2, vp2 = d.k_pool.reshape(R * bpr, C, 1, D), d.v_pool.reshape(R * bpr, C, 1, D)
+    pages_d, ip2d, lp2d, fp2d = pages.to(dev), ip2.to(dev), lp2.to(dev), fp2.to(dev)
+    out2 = torch.empty(R, n_rep, D, device=dev)
+    lse2 = torch.empty(R, n_rep, device=dev)
+    ws2 = (torch.empty(max(1, plan2.num_chunks), n_rep, D, device=dev),
+           torch.empty(max(1, plan2.num_chunks), n_rep, device=dev))
+
+    def block_granular():
+        pa.decode(plan2, d.q, kp2, vp2, pages_d, ip2d, lp2d, fp2d, s.scale, out2, lse2, ws2, None, stream)
+
+    # correctness guard against the oracle before timing
+    ref_rows, _ = oracle.selection_rows_ref(s.block_ids, C, s.kv_len, s.cap)
+    ref_o, _ = oracle.attention(s.q, s.k_pool, s.v_pool, ref_rows, ip, lp, fp, s.scale)
+    with torch.cuda.stream(stream):
+        token_exact()
+        block_granular()
+    stream.synchronize()
+    if not torch.equal(rows.cpu(), ref_rows):
+        raise SystemExit("bench: expanded rows disagree with the oracle; refusing to time")
+    for name, got in (("token_exact", out), ("block_granular", out2)):
+        err = float(abs(got.cpu().double().numpy() - ref_o).max())
+        if not err <= 2e-3:
+            raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}); refusing to time")
+
+    nbytes = R * per * D * 2 * s.k_pool.element_size()
+    res = {}
+    for name, fn in (("token_exact", token_exact), ("block_granular", block_granular)):
+        med, p10, p90 = _time_cold(fn, stream, flush, args.warmup, args.steps, args.graph)
+        res[name] = {"us_per_step_median": med, "us_p10": p10, "us_p90": p90, "kv_bytes_per_step": nbytes,
+                     "kv_read_gbs": nbytes / (med * 1e-6) / 1e9}
+    peak, _ = measured_peak()
+    main_arm = res["token_exact"]
+    line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main_arm["us_per_step_median"],
+            "unit": "us/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "block_sparse_selection", "requests": R, "num_qo_heads_per_request": n_rep,
+                       "head_dim": D, "block_size": C, "topk_blocks": topk, "kv_len": s.kv_len, "cap": s.cap,
+                       "rows_per_request": per, "kv_dtype": "float16", "l2": "512 MiB buffer read between steps",
+                       "cuda_graph": bool(args.graph), "token_exact_chunks": plan.num_chunks,
+                       "block_granular_chunks": plan2.num_chunks},
+            "arms": res, "pct_of_hbm_peak": 100.0 * main_arm["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "block_sparse_selection":
+        run_block_sparse(args)
     elif args.workload != "llama3_8b_32k":
         run_workload(args)
     else:

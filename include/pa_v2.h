@@ -74,6 +74,7 @@ typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 #define PA_DEVICE_BAD_PAGE      0x4  /* a page id outside [0, num_pages) */
 #define PA_DEVICE_BAD_INDPTR    0x8  /* o_indptr decreasing or outside [0, num_partials] */
 #define PA_DEVICE_WAIT_TIMEOUT  0x10 /* a bounded wait for staged K/V gave up */
+#define PA_DEVICE_BAD_BLOCK     0x20 /* a selected block id outside the scored range */
 
 /* Largest chunk count of any plan: the 65535 grid-z bound of the pages'
  * launch shape (PR #984, What changed 4), kept as a plan invariant. */
@@ -246,6 +247,50 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
                               int32_t* l1_last_page_len, int32_t* l1_first_page_offset,
                               int32_t* member_rows, int32_t* l0_out_rows, int32_t* l1_out_rows,
                               int32_t* merge_indptr);
+
+/* Block-sparse selections (sparse-paged-decode.md, issue #904: the paragraphs
+ * on selection_from_blocks and on the final block).  A model that scores
+ * blocks of `block_size` positions picks `topk` of the blocks 0 .. nb-2 of
+ * each request, nb = ceil(kv_len / block_size); the final block nb-1 (the
+ * query's own) is never scored and is always attended, its live
+ * kv_len - (nb-1)*block_size rows only.  The count of rows per request,
+ *   per_request = topk * block_size + kv_len - (nb-1)*block_size,
+ * depends on kv_len alone, so the page table's structure is host data while
+ * the rows themselves stay on the device.
+ *
+ * pa_selection_rows_per_request: per_request, or -1 when the arguments are
+ * invalid (block_size < 1, kv_len < 1, topk < 0 or topk > nb - 1). */
+int64_t pa_selection_rows_per_request(int32_t topk, int32_t block_size, int32_t kv_len);
+
+/* The page_size-1 CSR structure of a token-exact selection: indptr[r] =
+ * r * per_request, last_page_len[r] = 1 (0 when per_request is 0),
+ * first_page_offset[r] = 0.  HOST pointers: indptr [num_requests + 1],
+ * last_page_len and first_page_offset [num_requests].  PA_EINVAL for negative
+ * sizes, null pointers or num_requests * per_request above INT32_MAX. */
+pa_status pa_sparse_csr(int32_t num_requests, int64_t per_request, int32_t* indptr, int32_t* last_page_len,
+                        int32_t* first_page_offset);
+
+/* Expand the selected block ids into token rows, one device pass over the
+ * selected rows (O(selected)): request r's rows are, for each selected block
+ * j in the order given, r*request_stride + j*block_size + e for e in
+ * [0, block_size), then the final block's live rows
+ * r*request_stride + (nb-1)*block_size + e.  With a dense cache
+ * [B, H, Cap, D] viewed as the pool [B*H*Cap, 1, 1, D] and requests
+ * r = b*H + h, request_stride is the reserved capacity Cap (not the live
+ * length).  The result is the `indices` of a page_size-1 decode whose CSR
+ * structure pa_sparse_csr gives.
+ *   block_ids [num_requests, topk] device int32 (any order, e.g. an
+ *             argpartition output); may be null when topk == 0.
+ *   indices   [num_requests * per_request] device int32, written.
+ * A block id outside [0, nb-1) is not expanded: its rows are written as -1
+ * (which the decode kernels reject as a bad page id) and PA_DEVICE_BAD_BLOCK
+ * is OR-ed into *status when status is not null.  Host errors: PA_EINVAL for
+ * invalid sizes, request_stride < kv_len or a null `indices`; PA_EUNSUPPORTED
+ * when a row or the row count does not fit in int32.  Launched like the other
+ * kernels (programmatic dependent, asynchronous on cuda_stream). */
+pa_status pa_selection_from_blocks(const int32_t* block_ids, int32_t num_requests, int32_t topk,
+                                   int32_t block_size, int32_t kv_len, int64_t request_stride,
+                                   int32_t* indices, int32_t* status, void* cuda_stream);
 
 /* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
  * by every GPU that loads this library until the process exits. */

@@ -24,13 +24,15 @@ PA_OK, PA_EINVAL, PA_EGEOMETRY, PA_ECAPACITY, PA_EUNSUPPORTED, PA_ECUDA, PA_EOOB
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_V2_MAX_CHUNKS = 65535
 DEVICE_BAD_REQUEST, DEVICE_BAD_SLOT, DEVICE_BAD_PAGE, DEVICE_BAD_INDPTR, DEVICE_WAIT_TIMEOUT = 1, 2, 4, 8, 16
+DEVICE_BAD_BLOCK = 32
 
 KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 # Exported symbols of the C ABI (the header's declarations).
 ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
-               "pa_v2_cascade_detect", "pa_v2_cascade_split",
+               "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
+               "pa_selection_from_blocks",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -85,6 +87,12 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_decode_noalloc.restype = i32
         L.pa_merge_states.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
         L.pa_merge_states.restype = i32
+        L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
+        L.pa_selection_rows_per_request.restype = i64
+        L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
+        L.pa_sparse_csr.restype = i32
+        L.pa_selection_from_blocks.argtypes = [P, i32, i32, i32, i32, i64, P, P, P]
+        L.pa_selection_from_blocks.restype = i32
         L.pa_status_from_device.argtypes = [i32]
         L.pa_status_from_device.restype = i32
         L.pa_status_string.argtypes = [i32]
@@ -406,3 +414,45 @@ def decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_
     wv, wl = pa_v2_decode_partial(plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,
                                   sm_scale, wv, wl, status, stream, ri, ti)
     return pa_merge_states(wv, wl, oi, s.batch, out, lse2, status, stream)
+
+
+# ---------------------------------------------------------------------------
+# block-sparse selections
+# ---------------------------------------------------------------------------
+
+def pa_selection_rows_per_request(topk: int, block_size: int, kv_len: int) -> int:
+    """Rows each request's token-exact page table lists (pa_selection_rows_per_request); raises if invalid."""
+    n = int(lib().pa_selection_rows_per_request(int(topk), int(block_size), int(kv_len)))
+    if n < 0:
+        raise PaError(PA_EINVAL, "pa_selection_rows_per_request")
+    return n
+
+
+def pa_sparse_csr(num_requests: int, per_request: int):
+    """Host (indptr, last_page_len, first_page_offset) of a token-exact selection (pa_sparse_csr)."""
+    ip = torch.empty(num_requests + 1, dtype=torch.int32)
+    lp = torch.empty(max(num_requests, 1), dtype=torch.int32)
+    fp = torch.empty(max(num_requests, 1), dtype=torch.int32)
+    rc = lib().pa_sparse_csr(int(num_requests), int(per_request), ip.data_ptr(), lp.data_ptr(), fp.data_ptr())
+    if rc != PA_OK:
+        raise PaError(rc, "pa_sparse_csr")
+    return ip, lp[:num_requests], fp[:num_requests]
+
+
+def pa_selection_from_blocks(block_ids, block_size: int, kv_len: int, request_stride: int, indices=None,
+                             status=None, stream=None):
+    """Token rows of a block-sparse selection (pa_selection_from_blocks).  block_ids: device int32
+    [num_requests, topk].  Returns the device int32 indices [num_requests * per_request]."""
+    R, topk = block_ids.shape
+    per = pa_selection_rows_per_request(topk, block_size, kv_len)
+    if indices is None:
+        indices = torch.empty(max(1, R * per), dtype=torch.int32, device=block_ids.device)
+    if indices.numel() < R * per:
+        raise ValueError("indices too small for the selection")
+    rc = lib().pa_selection_from_blocks(_dev_ptr(block_ids, "block_ids", torch.int32) if topk else None, R, topk,
+                                        int(block_size), int(kv_len), int(request_stride),
+                                        _dev_ptr(indices, "indices", torch.int32),
+                                        _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_selection_from_blocks")
+    return indices[:R * per]

@@ -340,6 +340,50 @@ def scatter_dense(name: str, dense_k: Sequence[torch.Tensor], dense_v: Sequence[
         head_dim=D, scale=1.0 / math.sqrt(D))
 
 
+@dataclass
+class BlockSelection:
+    """A block-sparse decode input: a dense cache [B, H, cap, D] per side viewed as the page_size-1 pool
+    [B*H*cap, 1, 1, D], requests r = b*H + h (n_rep query heads each), and each request's selected block
+    ids -- distinct, unordered (as an argpartition returns them), drawn from the scored blocks
+    0 .. nb-2 of the live window kv_len, nb = ceil(kv_len / block_size).  Expanding the ids into rows is
+    the method's work and is not done here."""
+
+    q: torch.Tensor            # [R, n_rep, D] f32
+    k_pool: torch.Tensor       # [B*H*cap, 1, 1, D]
+    v_pool: torch.Tensor
+    block_ids: torch.Tensor    # [R, topk] int32
+    block_size: int
+    kv_len: int
+    cap: int
+    scale: float
+    name: str = "block_sparse_selection"
+
+    @property
+    def num_requests(self) -> int:
+        return self.q.shape[0]
+
+    def to(self, device) -> "BlockSelection":
+        return BlockSelection(self.q.to(device), self.k_pool.to(device), self.v_pool.to(device),
+                              self.block_ids.to(device), self.block_size, self.kv_len, self.cap, self.scale, self.name)
+
+
+def block_sparse_selection(seed: int = 1006, batch: int = 1, kv_heads: int = 4, n_rep: int = 16, head_dim: int = 128,
+                           kv_len: int = 32731, cap: int = 33024, block_size: int = 128, topk: int = 16,
+                           dtype: torch.dtype = torch.float16) -> BlockSelection:
+    """MiniMax-M3-shaped block-sparse decode (sparse-paged-decode.md: 64 query heads over 4 KV heads,
+    head_dim 128, block_size 128, topk_blocks 16).  kv_len leaves a partial final block (91 rows at the
+    defaults); cap, the reserved capacity, exceeds kv_len (33024 = 258 blocks, so the same allocation also
+    serves as a pool of 128-row pages)."""
+    gen = torch.Generator().manual_seed(seed)
+    R = batch * kv_heads
+    nb = -(-kv_len // block_size)
+    q = torch.randn(R, n_rep, head_dim, generator=gen, dtype=torch.float32)
+    k = torch.randn(R * cap, 1, 1, head_dim, generator=gen).to(dtype)
+    v = torch.randn(R * cap, 1, 1, head_dim, generator=gen).to(dtype)
+    ids = torch.stack([torch.randperm(nb - 1, generator=gen)[:topk] for _ in range(R)]).to(torch.int32)
+    return BlockSelection(q, k, v, ids, block_size, kv_len, cap, 1.0 / math.sqrt(head_dim))
+
+
 WORKLOADS = {
     "tiny_csr": tiny_csr,
     "llama3_8b_32k": llama3_8b_32k,
