@@ -19,6 +19,13 @@ expands the selected block ids of each request into the token rows a
 token-exact (page_size 1) page table lists, and ``selection_pages_ref`` gives
 the block-granular (page_size = block size) page list of a pool-backed cache.
 Both are plain loops over integers.
+
+Second K stream (sparse-paged-decode.md, the DSA paragraphs, third way out):
+``attention_extra`` scores token t as scale * (q . k[row_t][:dim] + q_extra .
+k_extra[row_t][:extra_dim]) and averages v[row_t][:dim]; rows resolve through
+the same page table as every other decode.  It gathers the rows with the
+pinned page resolution and uses f64 matrix products (a library primitive) for
+the two dot products and the weighted sum.
 """
 from __future__ import annotations
 
@@ -387,3 +394,87 @@ def selection_pages_ref(block_ids, block_size: int, kv_len: int, blocks_per_requ
     R = len(ids)
     return (torch.tensor(pages, dtype=torch.int32), torch.tensor(indptr, dtype=torch.int32),
             torch.full((R,), last, dtype=torch.int32), torch.zeros(R, dtype=torch.int32))
+
+
+def _rows_of(indices, indptr, last_page_len, first_page_offset, page_size, r):
+    n = seq_lens(indptr, last_page_len, first_page_offset, page_size)[r]
+    return resolve_rows(indices, indptr, first_page_offset, page_size, r, n)
+
+
+def _attend_extra(qr, qer, K, Ke, V, scale):
+    """qr [H, D], qer [H, E], K [n, D], Ke [n, E], V [n, D] (f64) -> out [H, D], lse2 [H]."""
+    H = qr.shape[0]
+    if K.shape[0] == 0:
+        return np.zeros((H, V.shape[1])), np.full(H, -np.inf)
+    s = scale * (qr @ K.T + qer @ Ke.T)                   # [H, n], natural-log units
+    m = s.max(axis=1, keepdims=True)
+    w = np.exp(s - m)
+    tot = w.sum(axis=1, keepdims=True)
+    return (w / tot) @ V, (m[:, 0] + np.log(tot[:, 0])) / np.log(2.0)
+
+
+def attention_extra(q, q_extra, k_pool, k_extra_pool, v_pool, dim: int, indices, indptr, last_page_len,
+                    first_page_offset, scale):
+    """Decode attention with a second K stream, every (request, query head): (out [B,Hq,dim], lse2 [B,Hq]).
+
+    Pools are [P, page_size, Hkv, width] tensors (width >= the dims used: a row's first `dim` elements are
+    its K (and, for v_pool, V) part; k_extra_pool's full width is the extra part).  Query head h reads KV
+    head h // (Hq / Hkv)."""
+    qf = torch.as_tensor(q).double().numpy()
+    qe = torch.as_tensor(q_extra).double().numpy()
+    B, Hq, D = qf.shape
+    assert D == dim
+    P, ps, Hkv, _ = k_pool.shape
+    G = Hq // Hkv
+    kd = k_pool.reshape(P * ps, Hkv, -1)
+    ked = k_extra_pool.reshape(P * ps, Hkv, -1)
+    vd = v_pool.reshape(P * ps, Hkv, -1)
+    out = np.zeros((B, Hq, dim))
+    lse = np.zeros((B, Hq))
+    ip, lp, fp = _i32(indptr), _i32(last_page_len), _i32(first_page_offset)
+    _check_table(ip, lp, fp, _i32(indices), ps, P, B)
+    for r in range(B):
+        rows = _rows_of(indices, indptr, last_page_len, first_page_offset, ps, r)
+        for kvh in range(Hkv):
+            K = kd[rows, kvh, :dim].double().numpy()
+            Ke = ked[rows, kvh, :].double().numpy()
+            V = vd[rows, kvh, :dim].double().numpy()
+            hs = slice(kvh * G, (kvh + 1) * G)
+            out[r, hs], lse[r, hs] = _attend_extra(qf[r, hs], qe[r, hs], K, Ke, V, scale)
+    return out, lse
+
+
+def partials_extra(q, q_extra, k_pool, k_extra_pool, v_pool, dim: int, indices, indptr, last_page_len,
+                   first_page_offset, scale, pages_per_chunk, request_indices, kv_tile_indices):
+    """Per-chunk normalized partials and lse2 of the second-K-stream decode.  Chunk (r, k) covers page
+    slots [k*ppc, min((k+1)*ppc, pages_r)), i.e. visible tokens [max(0, k*ppc*ps - fpo), min(seq_len,
+    (k+1)*ppc*ps - fpo))."""
+    qf = torch.as_tensor(q).double().numpy()
+    qe = torch.as_tensor(q_extra).double().numpy()
+    B, Hq, D = qf.shape
+    P, ps, Hkv, _ = k_pool.shape
+    G = Hq // Hkv
+    kd = k_pool.reshape(P * ps, Hkv, -1)
+    ked = k_extra_pool.reshape(P * ps, Hkv, -1)
+    vd = v_pool.reshape(P * ps, Hkv, -1)
+    ri, ti = _i32(request_indices), _i32(kv_tile_indices)
+    fpo = _i32(first_page_offset)
+    N = len(ri)
+    out = np.zeros((N, Hq, dim))
+    lse = np.zeros((N, Hq))
+    rows_of = {}
+    for c in range(N):
+        r, k = int(ri[c]), int(ti[c])
+        if r not in rows_of:
+            rows_of[r] = _rows_of(indices, indptr, last_page_len, first_page_offset, ps, r)
+        rows = rows_of[r]
+        t0 = max(0, k * pages_per_chunk * ps - int(fpo[r]))
+        t1 = min(len(rows), (k + 1) * pages_per_chunk * ps - int(fpo[r]))
+        sel = rows[t0:t1] if t1 > t0 else []
+        for kvh in range(Hkv):
+            K = kd[sel, kvh, :dim].double().numpy()
+            Ke = ked[sel, kvh, :].double().numpy()
+            V = vd[sel, kvh, :dim].double().numpy()
+            hs = slice(kvh * G, (kvh + 1) * G)
+            out[c, hs], lse[c, hs] = _attend_extra(qf[r, hs], qe[r, hs], K, Ke, V, scale)
+    return out, lse
