@@ -106,7 +106,7 @@ def measured_peak():
 
 
 KERNEL_SOURCES = {
-    "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_internal.cuh", "pa_device.cuh"],
+    "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_internal.cuh", "pa_device.cuh", "pa_mma.cuh"],
     "pa_v2_partial_simt_kernel": ["pa_partial_simt.cu", "pa_internal.cuh", "pa_device.cuh"],
 }
 

@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
       red[warp] = m;
       wsum_s[warp] = ws;
     }
+    __syncwarp();  // reconverge the per-lane branches before the aligned barrier
     __syncthreads();
     float M = red[0];
 #pragma unroll
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) red[warp] = m;
+    __syncwarp();
     __syncthreads();
     m = red[0];
 #pragma unroll

@@ -149,6 +149,7 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
     return PA_EINVAL;
   const int D = plan->head_dim;
   const int ps = plan->page_size;
+  if (D != 64 && D != 128) return PA_EUNSUPPORTED;
   if (num_pages * (int64_t)ps >= (1ll << 31)) return PA_EUNSUPPORTED;
   const int hpc = pa_v2_q_heads_per_cta(plan->num_qo_heads / plan->num_kv_heads, D, kv_dtype);
   if (hpc != plan->q_heads_per_cta) return PA_EINVAL;

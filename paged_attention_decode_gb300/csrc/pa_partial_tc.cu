@@ -40,82 +40,10 @@
 #include <cstdint>
 
 #include "pa_internal.cuh"
+#include "pa_mma.cuh"
 
 namespace pa {
 namespace {
-
-// ---- 16-bit element type traits -------------------------------------------
-
-template <typename T> struct TC;
-
-template <> struct TC<__half> {
-  __device__ __forceinline__ static float round(float x) { return __half2float(__float2half_rn(x)); }
-  __device__ __forceinline__ static uint32_t pack(float lo16, float hi16) {
-    __half2 h = __floats2half2_rn(lo16, hi16);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ __forceinline__ static unsigned short bits(float x) {
-    __half h = __float2half_rn(x);
-    return *reinterpret_cast<unsigned short*>(&h);
-  }
-  __device__ __forceinline__ static void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-};
-
-template <> struct TC<__nv_bfloat16> {
-  __device__ __forceinline__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-  __device__ __forceinline__ static uint32_t pack(float lo16, float hi16) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo16, hi16);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ __forceinline__ static unsigned short bits(float x) {
-    __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<unsigned short*>(&h);
-  }
-  __device__ __forceinline__ static void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Byte offset of 16-byte chunk `ch` (0 .. D/8-1) of stage row `row` in a
-// swizzled tile: 128-byte half rows, half-tiles of 16 rows (2 KB) each, chunk
-// index XOR (row mod 8) within the half row.
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-  return (uint32_t)((ch >> 3) * 2048 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
-}
 
 // ---- the kernel -------------------------------------------------------------
 

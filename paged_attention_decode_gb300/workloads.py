@@ -384,6 +384,50 @@ def block_sparse_selection(seed: int = 1006, batch: int = 1, kv_heads: int = 4, 
     return BlockSelection(q, k, v, ids, block_size, kv_len, cap, 1.0 / math.sqrt(head_dim))
 
 
+@dataclass
+class ExtraStreamBatch:
+    """Decode input for the second-K-stream kernel: a PagedBatch whose k_pool rows are RowStride wide (the
+    first `dim` elements are the key; v_pool may be the same tensor), plus q_extra and k_extra_pool."""
+
+    batch: PagedBatch
+    q_extra: torch.Tensor       # [B, Hq, extra]
+    k_extra_pool: torch.Tensor  # [P, page_size, Hkv, extra]
+    dim: int
+    shared_v: bool
+
+    def to(self, device) -> "ExtraStreamBatch":
+        b = self.batch.to(device)
+        if self.shared_v:
+            b.v_pool = b.k_pool
+        return ExtraStreamBatch(b, self.q_extra.to(device), self.k_extra_pool.to(device), self.dim, self.shared_v)
+
+
+def dsa_sparse_decode(seed: int = 1007, batch: int = 4, heads: int = 128, kv_lora_rank: int = 512,
+                      index_head_dim: int = 128, rope_dim: int = 64, kv_len: int = 8192, topk: int = 2048,
+                      dtype: torch.dtype = torch.bfloat16) -> ExtraStreamBatch:
+    """DSA-shaped token-exact sparse decode (sparse-paged-decode.md, the DSA paragraphs): per sequence a K
+    allocation [cap, kv_lora_rank + index_head_dim] (concat(kv_latent, indexer_key)) and a k_pe allocation
+    [cap, rope_dim], one KV head (MLA), `heads` query heads with q_latent [.., kv_lora_rank] and q_pe
+    [.., rope_dim]; the values are the latent rows (v_pool is k_pool).  Each request selects `topk` sorted
+    unique positions of its live window (an indexer's top-k), offset by the row stride cap between
+    sequences.  Scale 1/sqrt(128 + rope_dim): DeepSeek's qk head dim (nope 128 + rope)."""
+    gen = torch.Generator().manual_seed(seed)
+    cap = kv_len + 256
+    width = kv_lora_rank + index_head_dim
+    k = torch.randn(batch * cap, 1, 1, width, generator=gen).to(dtype)
+    kpe = torch.randn(batch * cap, 1, 1, rope_dim, generator=gen).to(dtype)
+    q = torch.randn(batch, heads, kv_lora_rank, generator=gen, dtype=torch.float32)
+    qe = torch.randn(batch, heads, rope_dim, generator=gen, dtype=torch.float32)
+    sel = [torch.randperm(kv_len, generator=gen)[:topk].sort().values + r * cap for r in range(batch)]
+    pb = PagedBatch(
+        name="dsa_sparse_decode", q=q, k_pool=k, v_pool=k, indices=torch.cat(sel).to(torch.int32),
+        indptr=torch.arange(0, (batch + 1) * topk, topk, dtype=torch.int32),
+        last_page_len=torch.ones(batch, dtype=torch.int32), first_page_offset=torch.zeros(batch, dtype=torch.int32),
+        seq_lens=[topk] * batch, page_size=1, num_qo_heads=heads, num_kv_heads=1, head_dim=kv_lora_rank,
+        scale=1.0 / math.sqrt(128 + rope_dim), meta={"cap": cap, "kv_len": kv_len})
+    return ExtraStreamBatch(pb, qe, kpe, kv_lora_rank, True)
+
+
 WORKLOADS = {
     "tiny_csr": tiny_csr,
     "llama3_8b_32k": llama3_8b_32k,

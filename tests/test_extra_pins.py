@@ -104,3 +104,20 @@ def test_partials_merge_to_the_whole(ppc):
     fin = np.isfinite(l)
     assert np.array_equal(np.isfinite(ml), fin)
     assert np.abs(mo - o).max() < 1e-12 and np.abs(ml[fin] - l[fin]).max() < 1e-12
+
+
+def test_dsa_shaped_inputs_against_sdpa():
+    """The DSA-shaped workload (128 heads, latent 512 + rope 64, values = latent rows, token-exact rows):
+    the oracle against SDPA on the concatenated rows, request by request."""
+    x = W.dsa_sparse_decode(batch=2, kv_len=1024, topk=256, heads=16)
+    b = x.batch
+    o, l = oracle.attention_extra(b.q, x.q_extra, b.k_pool, x.k_extra_pool, b.v_pool, x.dim, b.indices, b.indptr,
+                                  b.last_page_len, b.first_page_offset, b.scale)
+    for r in range(b.batch):
+        rows = b.indices[b.indptr[r]:b.indptr[r + 1]].long()
+        kc = torch.cat([b.k_pool[rows, 0, 0, :x.dim], x.k_extra_pool[rows, 0, 0]], dim=1).double()
+        v = b.v_pool[rows, 0, 0, :x.dim].double()
+        qc = torch.cat([b.q[r], x.q_extra[r]], dim=1).double()
+        ref = torch.nn.functional.scaled_dot_product_attention(qc[None], kc[None], v[None], scale=b.scale)[0]
+        assert float((torch.as_tensor(o[r]) - ref).abs().max()) < 1e-12
+        assert float((torch.as_tensor(l[r]) - torch.logsumexp(b.scale * qc @ kc.T, 1) / math.log(2.0)).abs().max()) < 1e-12

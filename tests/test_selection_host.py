@@ -43,3 +43,4 @@ def test_sparse_csr_rejects_overflow_and_negatives():
 
 def test_device_status_bit_for_bad_blocks_maps_to_eoob():
     assert pa.pa_status_from_device(pa.DEVICE_BAD_BLOCK) == pa.PA_EOOB
+
