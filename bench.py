@@ -470,9 +470,35 @@ def run_ours(args):
 
 
 def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
-    """Per step: one pinned H2D copy of q and the page table, the cached plan checked with
-    pa_v2_plan_matches, the decode launches (the same step as the device-timed region), one D2H copy of
-    out + lse, stream sync."""
+    """Per step, one call of the C ABI with host buffers (pa_v2_decode_host through the binding's
+    prepared HostStep): the cached plan checked against the step's page table, one host-to-device copy
+    of q and the page table from pinned memory, the partial and merge launches, one device-to-host copy
+    of out, lse2 and the status word, stream synchronisation.  The fused one-launch step (--fused) keeps
+    the per-array path: pa_v2_plan_matches, a pinned copy, pa_v2_decode, a copy back."""
+    if args.fused:
+        return run_e2e_fused(args, pa, plan, sets_cpu, sets, dev, stream, b0)
+    steps = []
+    for b, d in zip(sets_cpu, sets):
+        st = pa.HostStep(plan, d.k_pool, d.v_pool, stream)
+        st.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
+        steps.append(st)
+    for i in range(20):
+        steps[i % len(steps)].run(b0.scale)
+    n = args.e2e_steps
+    t0 = time.perf_counter()
+    for i in range(n):
+        steps[i % len(steps)].run(b0.scale)
+    el = time.perf_counter() - t0
+    kv_bytes = b0.kv_bytes()
+    return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
+            "h2d_bytes_per_step": steps[0].in_bytes, "d2h_bytes_per_step": steps[0].out_bytes,
+            "path": "per step: one pa_v2_decode_host call (plan check, 1 pinned H2D of q + page table, "
+                    + STEP_TWO + ", 1 D2H of status + out + lse2, stream sync); prepared ctypes arguments"}
+
+
+def run_e2e_fused(args, pa, plan, sets_cpu, sets, dev, stream, b0):
+    """The fused step end to end: pa_v2_plan_matches, one pinned H2D of q and the page table,
+    pa_v2_decode, one D2H of out + lse, stream sync."""
     B, Hq, D = b0.batch, b0.num_qo_heads, b0.head_dim
     # one pinned staging buffer per input set: [q (f32) | indices | indptr | lpl | fpo] as 32-bit words
     host_in, views = [], []
@@ -509,14 +535,8 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
             lp = dev_in[o:o + B]
             fp = dev_in[o + B:o + 2 * B]
             kp, vp = sets[i % len(sets)].k_pool, sets[i % len(sets)].v_pool
-            if args.fused:
-                pa.pa_v2_decode(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, out, lse, (wv, wl), counters, None,
-                                stream, ri, ti, oi)
-            elif plan.needs_merge:
-                pa.pa_v2_decode_partial(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, wv, wl, None, stream, ri, ti)
-                pa.pa_merge_states(wv, wl, oi, B, out, lse, None, stream)
-            else:
-                pa.pa_v2_decode_partial(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, out, lse, None, stream, ri, ti)
+            pa.pa_v2_decode(plan, q, kp, vp, idx, ip, lp, fp, b0.scale, out, lse, (wv, wl), counters, None,
+                            stream, ri, ti, oi)
             res_h.copy_(res_d, non_blocking=True)
         stream.synchronize()
 
@@ -530,8 +550,8 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     kv_bytes = b0.kv_bytes()
     return {"value": kv_bytes / (el / n) / 1e9, "unit": "GB/s", "us_per_step": el / n * 1e6, "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "per step: 1 pinned H2D (q + page table), pa_v2_plan_matches, "
-                    + (STEP_FUSED if args.fused else STEP_TWO) + ", 1 D2H (out + lse), stream sync; ctypes binding"}
+            "path": "per step: pa_v2_plan_matches, 1 pinned H2D (q + page table), " + STEP_FUSED
+                    + ", 1 D2H (out + lse), stream sync; ctypes binding"}
 
 
 def run_workload(args):

@@ -292,6 +292,39 @@ pa_status pa_selection_from_blocks(const int32_t* block_ids, int32_t num_request
                                    int32_t block_size, int32_t kv_len, int64_t request_stride,
                                    int32_t* indices, int32_t* status, void* cuda_stream);
 
+/* One whole decode step for callers whose per-step inputs (the query and the
+ * page table) are in host memory.  The pages have no counterpart to this call:
+ * it packages the step they time (plan built once outside the step; partial,
+ * then merge when needs_merge) with the host<->device traffic around it, so
+ * that a host-side caller makes one call, one host-to-device copy and one
+ * device-to-host copy per step.
+ *
+ * pa_v2_host_io_layout: byte sizes for a plan.  host_in [in_bytes] holds, as
+ * consecutive 4-byte words, q [batch, num_qo_heads, head_dim] f32, indices
+ * [num_indices] int32, indptr [batch+1], last_page_len [batch],
+ * first_page_offset [batch], then zeros up to in_bytes (the last 16 bytes are
+ * the device status slot, zeroed by the copy).  host_out [out_bytes] receives
+ * the status word (first 4 bytes of a 16-byte slot), out [batch, num_qo_heads,
+ * head_dim] f32 and lse2 [batch, num_qo_heads] f32.  dev_io is a device buffer
+ * of io_bytes (16-byte aligned) the call copies into and out of. */
+pa_status pa_v2_host_io_layout(const pa_v2_plan_t* plan, int64_t* in_bytes, int64_t* out_bytes,
+                               int64_t* io_bytes);
+
+/* pa_v2_decode_host: check that `plan` still matches the page table in host_in
+ * (PA_EGEOMETRY if not; nothing is launched), copy host_in to dev_io, run
+ * pa_v2_decode_partial (and pa_merge_states when plan->needs_merge, through
+ * workspace_v / workspace_lse sized by the plan), copy the status, out and
+ * lse2 to host_out, and synchronize `cuda_stream`.  host_in / host_out should
+ * be page-locked for the copies to be asynchronous.  k_pool, v_pool, the plan's
+ * device arrays (request_indices, kv_tile_indices, o_indptr) and the
+ * workspaces are device pointers as for the calls it makes.  Returns the first
+ * failing call's status, else pa_status_from_device(status word). */
+pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                            const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                            const int32_t* request_indices, const int32_t* kv_tile_indices,
+                            const int32_t* o_indptr, float sm_scale, float* workspace_v, float* workspace_lse,
+                            void* cuda_stream);
+
 /* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
  * by every GPU that loads this library until the process exits. */
 #define PA_V2_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -1,0 +1,94 @@
+// pa_host_step.cpp -- one whole decode step for callers whose per-step inputs
+// live in host memory: check the cached plan, copy the inputs in, run the
+// partial kernel (and the merge when the plan needs one), copy the outputs
+// back and wait, in one call.
+//
+// The pages time the decode with the plan built once outside the step and the
+// query cast once outside the timed region (PR #984, the commit extending
+// examples/page_gather_microbench.rs); what changes every step is the query
+// and the page table.  A caller that keeps those on the host otherwise pays
+// several API calls per step; here the inputs travel as one packed buffer in
+// one host-to-device copy and the outputs (with the device status word) in one
+// device-to-host copy, on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "pa_v2.h"
+
+namespace {
+
+int64_t round16(int64_t x) { return (x + 15) & ~int64_t{15}; }
+
+}  // namespace
+
+extern "C" pa_status pa_v2_host_io_layout(const pa_v2_plan_t* plan, int64_t* in_bytes, int64_t* out_bytes,
+                                          int64_t* io_bytes) {
+  if (!plan || !in_bytes || !out_bytes || !io_bytes || plan->batch < 0) return PA_EINVAL;
+  const int64_t B = plan->batch;
+  const int64_t rows = B * plan->num_qo_heads;
+  const int64_t words = rows * plan->head_dim + plan->num_indices + (B + 1) + 2 * B;
+  *in_bytes = round16(words * 4) + 16;                     // inputs, then a zeroed 16-byte status slot
+  *out_bytes = 16 + rows * plan->head_dim * 4 + rows * 4;  // the status slot, out, lse2
+  *io_bytes = *in_bytes - 16 + *out_bytes;                 // the status slot is shared
+  return PA_OK;
+}
+
+extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                                       const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                       const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                       const int32_t* o_indptr, float sm_scale, float* workspace_v,
+                                       float* workspace_lse, void* cuda_stream) {
+  int64_t in_bytes = 0, out_bytes = 0, io_bytes = 0;
+  if (pa_v2_host_io_layout(plan, &in_bytes, &out_bytes, &io_bytes) != PA_OK) return PA_EINVAL;
+  if (!host_in || !host_out || !dev_io || (reinterpret_cast<uintptr_t>(dev_io) & 15u)) return PA_EINVAL;
+  if (plan->needs_merge && (!workspace_v || !workspace_lse || !o_indptr)) return PA_EINVAL;
+  const int32_t B = plan->batch;
+  const int64_t rows = (int64_t)B * plan->num_qo_heads;
+  const int64_t q_words = rows * plan->head_dim;
+
+  // the packed host inputs: q | indices | indptr | last_page_len | first_page_offset (4-byte words)
+  const int32_t* h_words = static_cast<const int32_t*>(host_in);
+  const int32_t* h_indptr = h_words + q_words + plan->num_indices;
+  const int32_t* h_lpl = h_indptr + B + 1;
+  const int32_t* h_fpo = h_lpl + B;
+  if (!pa_v2_plan_matches(plan, h_indptr, h_lpl, h_fpo, B)) return PA_EGEOMETRY;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  unsigned char* io = static_cast<unsigned char*>(dev_io);
+  if (cudaMemcpyAsync(io, host_in, (size_t)in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return PA_ECUDA;
+
+  const float* q = reinterpret_cast<const float*>(io);
+  const int32_t* indices = reinterpret_cast<const int32_t*>(io) + q_words;
+  const int32_t* indptr = indices + plan->num_indices;
+  const int32_t* lpl = indptr + B + 1;
+  const int32_t* fpo = lpl + B;
+  unsigned char* out_region = io + in_bytes - 16;  // the status slot the copy above zeroed, then out, lse2
+  int32_t* status = reinterpret_cast<int32_t*>(out_region);
+  float* out = reinterpret_cast<float*>(out_region + 16);
+  float* lse = out + q_words;
+
+  pa_status rc;
+  if (plan->needs_merge) {
+    rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
+                              fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse, status,
+                              cuda_stream);
+    if (rc == PA_OK)
+      rc = pa_merge_states(workspace_v, workspace_lse, o_indptr, B, plan->num_chunks, plan->num_qo_heads,
+                           plan->head_dim, out, lse, status, cuda_stream);
+  } else {
+    rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
+                              fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cuda_stream);
+  }
+  if (rc != PA_OK) {
+    cudaStreamSynchronize(stream);  // the input copy may still be reading host_in
+    return rc;
+  }
+  if (cudaMemcpyAsync(host_out, out_region, (size_t)out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PA_ECUDA;
+  int32_t word = 0;
+  std::memcpy(&word, host_out, sizeof(word));
+  return pa_status_from_device(word);
+}

@@ -32,7 +32,7 @@ KV_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF
 ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan", "pa_v2_plan_matches",
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
                "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
-               "pa_selection_from_blocks",
+               "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_decode_noalloc.restype = i32
         L.pa_merge_states.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
         L.pa_merge_states.restype = i32
+        L.pa_v2_host_io_layout.argtypes = [PP, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        L.pa_v2_host_io_layout.restype = i32
+        L.pa_v2_decode_host.argtypes = [PP, P, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
+        L.pa_v2_decode_host.restype = i32
         L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
         L.pa_selection_rows_per_request.restype = i64
         L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
@@ -456,3 +460,65 @@ def pa_selection_from_blocks(block_ids, block_size: int, kv_len: int, request_st
     if rc != PA_OK:
         raise PaError(rc, "pa_selection_from_blocks")
     return indices[:R * per]
+
+
+# ---------------------------------------------------------------------------
+# one step from host buffers
+# ---------------------------------------------------------------------------
+
+def pa_v2_host_io_layout(plan: Plan) -> tuple[int, int, int]:
+    """(in_bytes, out_bytes, io_bytes) of pa_v2_decode_host for `plan`."""
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().pa_v2_host_io_layout(ctypes.byref(plan.struct), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_host_io_layout")
+    return a.value, b.value, c.value
+
+
+class HostStep:
+    """pa_v2_decode_host with its buffers allocated once and its C arguments prepared once.
+
+    pack(q, indices, indptr, last_page_len, first_page_offset) writes a step's host inputs into the pinned
+    input buffer (or pass prepacked=True to run() after filling `host_in` yourself); run() makes the one
+    C call and returns (out [B, Hq, D], lse2 [B, Hq]) as views of the pinned output buffer."""
+
+    def __init__(self, plan: Plan, k_pool, v_pool, stream=None):
+        s = plan.struct
+        self.plan = plan
+        dev = k_pool.device
+        self.in_bytes, self.out_bytes, self.io_bytes = pa_v2_host_io_layout(plan)
+        self.host_in = torch.zeros(self.in_bytes, dtype=torch.uint8).pin_memory()
+        self.host_out = torch.zeros(self.out_bytes, dtype=torch.uint8).pin_memory()
+        self.dev_io = torch.empty(self.io_bytes, dtype=torch.uint8, device=dev)
+        ri, ti, oi = plan.device_arrays(dev)
+        self.ws = (torch.empty(max(1, s.num_chunks), s.num_qo_heads, s.head_dim, device=dev),
+                   torch.empty(max(1, s.num_chunks), s.num_qo_heads, device=dev))
+        rows = s.batch * s.num_qo_heads
+        self.words_in = self.host_in.view(torch.int32)
+        self.q_words = rows * s.head_dim
+        self.out = self.host_out[16:16 + rows * s.head_dim * 4].view(torch.float32).view(s.batch, s.num_qo_heads,
+                                                                                           s.head_dim)
+        self.lse = self.host_out[16 + rows * s.head_dim * 4:].view(torch.float32).view(s.batch, s.num_qo_heads)
+        self._keep = (k_pool, v_pool, ri, ti, oi, stream)
+        self._fn = lib().pa_v2_decode_host
+        self._args = (ctypes.byref(s), self.host_in.data_ptr(), self.host_out.data_ptr(), self.dev_io.data_ptr(),
+                      _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"), KV_DTYPES[k_pool.dtype],
+                      k_pool.shape[0], ri.data_ptr(), ti.data_ptr(), oi.data_ptr())
+        self._tail = (self.ws[0].data_ptr(), self.ws[1].data_ptr(), _stream(stream))
+
+    def pack(self, q, indices, indptr, last_page_len, first_page_offset):
+        """Copy one step's inputs (host tensors) into the pinned input buffer."""
+        w = self.words_in
+        o = 0
+        for t in (q.reshape(-1).view(torch.int32), indices, indptr, last_page_len, first_page_offset):
+            n = t.numel()
+            w[o:o + n] = t.reshape(-1).to(torch.int32)
+            o += n
+        w[o:] = 0
+
+    def run(self, sm_scale: float):
+        rc = self._fn(*self._args, float(sm_scale), *self._tail)
+        if rc != PA_OK:
+            raise PaError(rc, "pa_v2_decode_host")
+        return self.out, self.lse
+

@@ -215,3 +215,14 @@ def test_plan_matches_predicate():
     bad = b.last_page_len.clone()
     bad[0] = 0
     assert not pa.pa_v2_plan_matches(p, b.indptr, bad, b.first_page_offset)
+
+
+def test_host_io_layout_sizes():
+    b = W.tiny_csr()
+    plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
+                         b.num_kv_heads, b.head_dim, pa.PA_F32, 8, b.ppc_override, b.seq_lens)
+    i, o, io = pa.pa_v2_host_io_layout(plan)
+    words = b.q.numel() + b.indices.numel() + (b.batch + 1) + 2 * b.batch
+    assert i == -(-words * 4 // 16) * 16 + 16 and i % 16 == 0
+    assert o == 16 + b.q.numel() * 4 + b.batch * b.num_qo_heads * 4
+    assert io == i - 16 + o

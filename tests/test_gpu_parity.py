@@ -364,3 +364,53 @@ def test_autotune_times_candidates_and_tuned_plan_is_exact(fused):
     assert res.pages_per_chunk in res.times_us
     assert all(t > 0 for t in res.times_us.values())
     check_batch(b, override=res.pages_per_chunk)
+
+
+# ---------------------------------------------------------------------------
+# one step from host buffers (pa_v2_decode_host)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_csr", "sliding_window_batch", "nomerge"])
+def test_host_step_matches_the_device_path(name):
+    if name == "nomerge":
+        b = W.make_batch("nomerge", [40, 17, 0], [0, 3, 0], 16, 8, 2, 128, torch.float16, seed=23)
+        plan = make_plan(b, target=1)
+        assert not plan.needs_merge
+    else:
+        b = W.WORKLOADS[name]()
+        plan = make_plan(b)
+    d = b.to("cuda")
+    step = pa.HostStep(plan, d.k_pool, d.v_pool)
+    step.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
+    for _ in range(2):                                  # the status slot is re-zeroed by every copy
+        o, l = step.run(b.scale)
+    ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                    b.first_page_offset, b.scale)
+    assert_close(o.clone(), l.clone(), ref_o, ref_l, f"host step {name}")
+    o2, l2 = pa.decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len, d.first_page_offset,
+                       b.scale)
+    assert torch.equal(o2.cpu(), o) and torch.equal(l2.cpu(), l)
+
+
+def test_host_step_refuses_a_stale_plan_and_reports_bad_pages():
+    b = W.make_batch("hs", [100, 60], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
+    plan = make_plan(b, target=16)
+    d = b.to("cuda")
+    step = pa.HostStep(plan, d.k_pool, d.v_pool)
+    grown = W.make_batch("hs", [100, 90], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
+    step.pack(grown.q, grown.indices[:b.indices.numel()], grown.indptr, grown.last_page_len,
+              grown.first_page_offset)
+    with pytest.raises(pa.PaError) as e:
+        step.run(b.scale)
+    assert e.value.status == pa.PA_EGEOMETRY
+    bad = b.indices.clone()
+    bad[2] = b.num_pages
+    step.pack(b.q, bad, b.indptr, b.last_page_len, b.first_page_offset)
+    with pytest.raises(pa.PaError) as e:
+        step.run(b.scale)
+    assert e.value.status == pa.PA_EOOB
+    step.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
+    o, l = step.run(b.scale)                            # a clean step afterwards is exact again
+    ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                    b.first_page_offset, b.scale)
+    assert_close(o.clone(), l.clone(), ref_o, ref_l, "host step after errors")
