@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--context", type=int, default=32768)
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix",
-                             "tiny_csr", "block_sparse_selection"],
+                             "tiny_csr", "block_sparse_selection", "crossover"],
                     help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
                          "(cold L2 for every step)")
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
@@ -825,10 +825,93 @@ def run_block_sparse(args):
     print(json.dumps(line), flush=True)
 
 
+def run_crossover(args):
+    """The pages' performance sweep on GB300 (PR #984, the M1 Ultra validation report; issue #898,
+    Performance validation): batch {1, 4, 8} x context {1024, 4096, 16384, 32768}, Llama-3-8B heads
+    (Hq 32, Hkv 8, D 128), fp16 pools, page_size 16, random physical pages.  Arms per cell, each a
+    CUDA graph of one step after a 512 MiB L2 flush, median of `--steps`:
+      v2           this library's decode (pa_v2_decode_partial + pa_merge_states)
+      gather_sdpa  gather the pages into contiguous [B, Hkv, ctx, D] K and V (torch index_select), then
+                   torch's scaled_dot_product_attention (the pages' gather-then-SDPA path)
+      contiguous   scaled_dot_product_attention on K and V already contiguous (the lower bound of the
+                   gather path: no gather)
+    The query reaches each arm in the form it consumes (f32 for v2, fp16 for SDPA), cast outside the
+    timed region."""
+    from paged_attention_decode_gb300 import build as pa_build
+    from paged_attention_decode_gb300 import pa_v2 as pa
+    from paged_attention_decode_gb300 import workloads as W
+
+    pa_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    F = torch.nn.functional
+    Hq, Hkv, D, ps = 32, 8, 128, 16
+    cells = []
+    for B in (1, 4, 8):
+        for ctx in (1024, 4096, 16384, 32768):
+            b = W.make_batch(f"crossover_b{B}_c{ctx}", [ctx] * B, [0] * B, ps, Hq, Hkv, D, torch.float16,
+                             seed=1100 + B * 7 + ctx // 1024)
+            d = b.to(dev)
+            dt = pa.KV_DTYPES[b.dtype]
+            plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, ps, Hq, Hkv, D, dt,
+                                 pa.pa_v2_default_target_ctas(Hq, Hkv, D, ps, dt), 0, b.seq_lens)
+            out = torch.empty(B, Hq, D, device=dev)
+            lse = torch.empty(B, Hq, device=dev)
+            ws = (torch.empty(max(1, plan.num_chunks), Hq, D, device=dev),
+                  torch.empty(max(1, plan.num_chunks), Hq, device=dev))
+            pages = ctx // ps
+            idx = d.indices.view(B, pages).long()
+            q16 = d.q.to(torch.float16).view(B, Hq, 1, D)
+            kc = d.k_pool[idx].reshape(B, pages * ps, Hkv, D).transpose(1, 2).contiguous()
+            vc = d.v_pool[idx].reshape(B, pages * ps, Hkv, D).transpose(1, 2).contiguous()
+
+            def v2():
+                pa.decode(plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                          d.first_page_offset, b.scale, out, lse, ws, None, stream)
+
+            def gather_sdpa():
+                k = d.k_pool[idx].reshape(B, pages * ps, Hkv, D).transpose(1, 2)
+                v = d.v_pool[idx].reshape(B, pages * ps, Hkv, D).transpose(1, 2)
+                return F.scaled_dot_product_attention(q16, k, v, scale=b.scale, enable_gqa=True)
+
+            def contiguous():
+                return F.scaled_dot_product_attention(q16, kc, vc, scale=b.scale, enable_gqa=True)
+
+            with torch.cuda.stream(stream):
+                v2()
+                ref = contiguous()
+            stream.synchronize()
+            err = float((out - ref.view(B, Hq, D).float()).abs().max())
+            if not err <= 2e-2:
+                raise SystemExit(f"bench: crossover B={B} ctx={ctx}: v2 and SDPA disagree ({err:.3e})")
+            cell = {"batch": B, "context": ctx, "pages_per_chunk": plan.pages_per_chunk,
+                    "chunks": plan.num_chunks, "merge": bool(plan.needs_merge)}
+            for name, fn in (("v2", v2), ("gather_sdpa", gather_sdpa), ("contiguous", contiguous)):
+                med, p10, p90 = _time_cold(fn, stream, flush, args.warmup, args.steps, args.graph)
+                cell[name + "_us"] = round(med, 2)
+            cell["v2_over_gather"] = round(cell["gather_sdpa_us"] / cell["v2_us"], 3)
+            cell["v2_over_contiguous"] = round(cell["contiguous_us"] / cell["v2_us"], 3)
+            cells.append(cell)
+            del b, d, kc, vc
+            torch.cuda.empty_cache()
+    line = {"metric": "decode us/step by batch and context (median, cold L2): v2 vs gather-then-SDPA vs "
+                      "contiguous SDPA", "unit": "us/step", "higher_is_better": False, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+            "config": {"workload": "crossover", "num_qo_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
+                       "page_size": ps, "kv_dtype": "float16", "l2": "512 MiB buffer read between steps",
+                       "cuda_graph": bool(args.graph)},
+            "cells": cells}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "crossover":
+        run_crossover(args)
     elif args.workload == "block_sparse_selection":
         run_block_sparse(args)
     elif args.workload != "llama3_8b_32k":
