@@ -118,9 +118,9 @@ typedef struct pa_v2_plan_t {
 
 /* Query heads one CTA serves for GQA group size `group_size`: up to 16 for
  * f16/bf16 pools (tensor-core kernel), up to 8 for f32 pools (CUDA-core
- * kernel).  The plan and the launcher both call this, so the CTA count and the
- * grid cannot drift apart (PR #984, What changed 2).  Returns 0 for an
- * unsupported shape. */
+ * kernel); head_dim 512 (the second-K-stream kernel, f16/bf16) up to 16.  The
+ * plan and the launcher both call this, so the CTA count and the grid cannot
+ * drift apart (PR #984, What changed 2).  Returns 0 for an unsupported shape. */
 int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype);
 
 /* Occupancy-derived CTA target for `device`: SM count times the partial
@@ -175,7 +175,7 @@ int32_t pa_v2_plan_matches(const pa_v2_plan_t* plan, const int32_t* indptr,
  * (num_pages * page_size < 2^31).  num_indices: length of `indices`.
  * status: nullable device int32 receiving PA_DEVICE_* bits.
  * Supported: head_dim 64 or 128; kv_dtype f32, f16, bf16; page_size 1..16 or
- * a multiple of 16 up to 256. */
+ * a multiple of 16 up to 256 (head_dim 512 plans: pa_v2_decode_partial_extra). */
 pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,
                                const void* v_pool, int32_t kv_dtype, int64_t num_pages,
                                const int32_t* indices, int64_t num_indices, const int32_t* indptr,
@@ -247,6 +247,41 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
                               int32_t* l1_last_page_len, int32_t* l1_first_page_offset,
                               int32_t* member_rows, int32_t* l0_out_rows, int32_t* l1_out_rows,
                               int32_t* merge_indptr);
+
+/* Partial attention with a second K stream (sparse-paged-decode.md, issue
+ * #904: the DSA paragraphs, third way out -- "a row stride plus a second K
+ * stream").  The score of visible token t (resolved through the page table
+ * exactly as in pa_v2_decode_partial) for query head h of kv head kvh is
+ *   scale * (q[h] . K_t[0:Dim]) + scale * (q_extra[h] . E_t[0:ExtraDim])
+ * and the output is the softmax-weighted sum of V_t[0:Dim], with
+ *   K_t = k_pool       + ((page*page_size + e) * num_kv_heads + kvh) * k_row_stride
+ *   E_t = k_extra_pool + (same row) * k_extra_row_stride
+ *   V_t = v_pool       + (same row) * v_row_stride      (elements of kv_dtype)
+ * Row strides (RowStride) may exceed the dims read: the DSA K buffer holds
+ * concat(kv_latent, indexer_key) per row and only the latent part is a key.
+ * For MLA the values are the latent rows: pass v_pool == k_pool with the same
+ * stride and each row is read once.  CUDA-core kernel (f32 arithmetic).
+ *   plan        from pa_v2_plan with head_dim = Dim = 512 (16 query heads per
+ *               CTA, pa_v2_q_heads_per_cta); stack_members and out_row_step 1.
+ *   q [batch, num_qo_heads, 512] f32 (16-byte aligned), q_extra [batch,
+ *   num_qo_heads, 64] f32 (8-byte aligned).
+ *   extra_dim   must be 64 (ExtraDim).
+ *   strides     in elements, multiples of 8, k/v >= 512, extra >= 64; pools
+ *               16-byte aligned.
+ *   v_out [num_chunks, num_qo_heads, 512] f32 (16-byte aligned) and lse2_out
+ *   [num_chunks, num_qo_heads] f32 as pa_v2_decode_partial; pa_merge_states
+ *   combines them.
+ * kv_dtype f16 or bf16.  Other arguments, device checks and errors as
+ * pa_v2_decode_partial; PA_EUNSUPPORTED for other dims or dtypes. */
+pa_status pa_v2_decode_partial_extra(const pa_v2_plan_t* plan, const float* q, const float* q_extra,
+                                     const void* k_pool, int64_t k_row_stride, const void* v_pool,
+                                     int64_t v_row_stride, const void* k_extra_pool, int64_t k_extra_row_stride,
+                                     int32_t extra_dim, int32_t kv_dtype, int64_t num_pages,
+                                     const int32_t* indices, int64_t num_indices, const int32_t* indptr,
+                                     const int32_t* last_page_len, const int32_t* first_page_offset,
+                                     const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                     float sm_scale, float* v_out, float* lse2_out, int32_t* status,
+                                     void* cuda_stream);
 
 /* Block-sparse selections (sparse-paged-decode.md, issue #904: the paragraphs
  * on selection_from_blocks and on the final block).  A model that scores

@@ -389,6 +389,9 @@ int occupancy_partial_simt(int kv_dtype, int head_dim, int hpc, int* blocks_per_
 int launch_partial_tc(const LaunchArgs& a, bool use_tma);
 int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int* blocks_per_sm);
 
+// Second-K-stream kernel (head_dim 512 + extra 64; f16 / bf16 pools).
+int occupancy_partial_extra(int kv_dtype, int* blocks_per_sm);
+
 // True when the tensor-core kernel stages this page size with TMA.
 inline bool tc_uses_tma(int page_size) {
   return page_size % 8 == 0 && (page_size <= kStageRows || page_size % kStageRows == 0);

@@ -89,7 +89,10 @@ bool use_tensor_cores(int kv_dtype, int kernel) {
 }  // namespace pa
 
 extern "C" int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype) {
-  if (group_size < 1 || (head_dim != 64 && head_dim != 128)) return 0;
+  if (group_size < 1) return 0;
+  if (head_dim == 512)  // the second-K-stream kernel (pa_v2_decode_partial_extra): f16 / bf16 only
+    return kv_dtype == PA_F16 || kv_dtype == PA_BF16 ? (group_size < 16 ? group_size : 16) : 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
   if (kv_dtype == PA_F16 || kv_dtype == PA_BF16) return group_size < 16 ? group_size : 16;
   if (kv_dtype == PA_F32) return group_size < 8 ? group_size : 8;
   return 0;
@@ -108,7 +111,8 @@ extern "C" pa_status pa_v2_default_target_ctas(int32_t device, int32_t num_qo_he
   if (device != prev && cudaSetDevice(device) != cudaSuccess) return PA_ECUDA;
   int sms = 0, per_sm = 0, rc = PA_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess) {
-    rc = pa::use_tensor_cores(kv_dtype, 0)
+    rc = head_dim == 512 ? pa::occupancy_partial_extra(kv_dtype, &per_sm)
+         : pa::use_tensor_cores(kv_dtype, 0)
              ? pa::occupancy_partial_tc(kv_dtype, head_dim, hpc, pa::tc_uses_tma(page_size), &per_sm)
              : pa::occupancy_partial_simt(kv_dtype, head_dim, hpc, &per_sm);
   }
@@ -149,7 +153,7 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
     return PA_EINVAL;
   const int D = plan->head_dim;
   const int ps = plan->page_size;
-  if (D != 64 && D != 128) return PA_EUNSUPPORTED;
+  if (D != 64 && D != 128) return PA_EUNSUPPORTED;  // head_dim 512 plans run pa_v2_decode_partial_extra
   if (num_pages * (int64_t)ps >= (1ll << 31)) return PA_EUNSUPPORTED;
   const int hpc = pa_v2_q_heads_per_cta(plan->num_qo_heads / plan->num_kv_heads, D, kv_dtype);
   if (hpc != plan->q_heads_per_cta) return PA_EINVAL;

@@ -33,6 +33,7 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
                "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
+               "pa_v2_decode_partial_extra",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -91,6 +92,9 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_host_io_layout.restype = i32
         L.pa_v2_decode_host.argtypes = [PP, P, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
         L.pa_v2_decode_host.restype = i32
+        L.pa_v2_decode_partial_extra.argtypes = [PP, P, P, P, i64, P, i64, P, i64, i32, i32, i64, P, i64, P, P, P,
+                                                 P, P, f32, P, P, P, P]
+        L.pa_v2_decode_partial_extra.restype = i32
         L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
         L.pa_selection_rows_per_request.restype = i64
         L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
@@ -521,4 +525,62 @@ class HostStep:
         if rc != PA_OK:
             raise PaError(rc, "pa_v2_decode_host")
         return self.out, self.lse
+
+
+# ---------------------------------------------------------------------------
+# second K stream (MLA / DSA)
+# ---------------------------------------------------------------------------
+
+def pa_v2_decode_partial_extra(plan: Plan, q, q_extra, k_pool, v_pool, k_extra_pool, indices, indptr,
+                               last_page_len, first_page_offset, sm_scale: float, v_out=None, lse2_out=None,
+                               status=None, stream=None, request_indices=None, kv_tile_indices=None):
+    """Partial kernel with a second K stream (pa_v2_decode_partial_extra).
+
+    Pools are device tensors [P, page_size, Hkv, width] whose last dimension is the row stride: k_pool and
+    v_pool rows hold the 512-wide key / value part first (v_pool may be k_pool itself: MLA), k_extra_pool
+    rows the 64-wide extra key.  Returns (v_out [N, Hq, 512], lse2_out [N, Hq])."""
+    s = plan.struct
+    dev = q.device
+    if request_indices is None or kv_tile_indices is None:
+        request_indices, kv_tile_indices, _ = plan.device_arrays(dev)
+    if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_extra_pool.dtype != k_pool.dtype:
+        raise ValueError("k_pool, v_pool and k_extra_pool must share a 16-bit dtype")
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool), ("k_extra_pool", k_extra_pool)):
+        if t.dim() != 4 or tuple(t.shape[1:3]) != (s.page_size, s.num_kv_heads) or t.shape[0] != k_pool.shape[0]:
+            raise ValueError(f"{name} must be [P, {s.page_size}, {s.num_kv_heads}, width]")
+    if v_out is None:
+        v_out = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(max(s.num_chunks, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+    rc = lib().pa_v2_decode_partial_extra(
+        ctypes.byref(s), _dev_ptr(q, "q", torch.float32), _dev_ptr(q_extra, "q_extra", torch.float32),
+        _dev_ptr(k_pool, "k_pool"), k_pool.shape[3], _dev_ptr(v_pool, "v_pool"), v_pool.shape[3],
+        _dev_ptr(k_extra_pool, "k_extra_pool"), k_extra_pool.shape[3], q_extra.shape[-1], KV_DTYPES[k_pool.dtype],
+        k_pool.shape[0], _dev_ptr(indices, "indices", torch.int32), indices.numel(),
+        _dev_ptr(indptr, "indptr", torch.int32), _dev_ptr(last_page_len, "last_page_len", torch.int32),
+        _dev_ptr(first_page_offset, "first_page_offset", torch.int32),
+        _dev_ptr(request_indices, "request_indices", torch.int32),
+        _dev_ptr(kv_tile_indices, "kv_tile_indices", torch.int32), float(sm_scale),
+        _dev_ptr(v_out, "v_out", torch.float32), _dev_ptr(lse2_out, "lse2_out", torch.float32),
+        _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_decode_partial_extra")
+    return v_out, lse2_out
+
+
+def decode_extra(plan: Plan, q, q_extra, k_pool, v_pool, k_extra_pool, indices, indptr, last_page_len,
+                 first_page_offset, sm_scale: float, out=None, lse2=None, workspace=None, status=None, stream=None):
+    """One second-K-stream decode step: pa_v2_decode_partial_extra, then pa_merge_states when the plan needs
+    it.  Returns (out [B, Hq, 512], lse2 [B, Hq])."""
+    s = plan.struct
+    ri, ti, oi = plan.device_arrays(q.device)
+    if not s.needs_merge:
+        v, l = pa_v2_decode_partial_extra(plan, q, q_extra, k_pool, v_pool, k_extra_pool, indices, indptr,
+                                          last_page_len, first_page_offset, sm_scale, out, lse2, status, stream,
+                                          ri, ti)
+        return v[:s.batch], l[:s.batch]
+    wv, wl = workspace if workspace is not None else (None, None)
+    wv, wl = pa_v2_decode_partial_extra(plan, q, q_extra, k_pool, v_pool, k_extra_pool, indices, indptr,
+                                        last_page_len, first_page_offset, sm_scale, wv, wl, status, stream, ri, ti)
+    return pa_merge_states(wv, wl, oi, s.batch, out, lse2, status, stream)
 

@@ -1,0 +1,97 @@
+"""GPU: the second-K-stream partial kernel (pa_v2_decode_partial_extra) against the oracle -- partials
+chunk by chunk and the merged result -- on MLA-shaped (values = latent rows) and separate-V inputs,
+token-exact and paged tables, f16 and bf16, and the DSA-shaped workload."""
+import math
+
+import pytest
+import torch
+
+import oracle
+from paged_attention_decode_gb300 import pa_v2 as pa
+from paged_attention_decode_gb300 import workloads as W
+from parity_helpers import assert_close
+
+pytestmark = pytest.mark.gpu
+
+D, E = 512, 64
+
+
+def _paged(seq, fpo, ps, Hq, Hkv, dtype, seed, k_width=640, v_width=None, shared_v=True):
+    """A paged batch whose k rows are k_width wide (key = first 512), extra rows 64 wide."""
+    b = W.make_batch("extra", seq, fpo, ps, Hq, Hkv, k_width, dtype, seed=seed)
+    gen = torch.Generator().manual_seed(seed + 7)
+    b.q = torch.randn(len(seq), Hq, D, generator=gen)
+    qe = torch.randn(len(seq), Hq, E, generator=gen)
+    ke = torch.randn(b.k_pool.shape[0], ps, Hkv, E, generator=gen).to(dtype)
+    if shared_v:
+        b.v_pool = b.k_pool
+    elif v_width is not None:
+        b.v_pool = torch.randn(b.k_pool.shape[0], ps, Hkv, v_width, generator=gen).to(dtype)
+    b.head_dim = D
+    return W.ExtraStreamBatch(b, qe, ke, D, shared_v)
+
+
+def _check(x, target=None, override=0, scale=None):
+    b = x.batch
+    dt = pa.KV_DTYPES[b.dtype]
+    tgt = target or pa.pa_v2_default_target_ctas(b.num_qo_heads, b.num_kv_heads, D, b.page_size, dt)
+    plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
+                         b.num_kv_heads, D, dt, tgt, override, b.seq_lens)
+    scale = scale or 1.0 / math.sqrt(D + E)
+    d = x.to("cuda")
+    db = d.batch
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    v, l = pa.pa_v2_decode_partial_extra(plan, db.q, d.q_extra, db.k_pool, db.v_pool, d.k_extra_pool, db.indices,
+                                         db.indptr, db.last_page_len, db.first_page_offset, scale, status=status)
+    out, lse = pa.decode_extra(plan, db.q, d.q_extra, db.k_pool, db.v_pool, d.k_extra_pool, db.indices, db.indptr,
+                               db.last_page_len, db.first_page_offset, scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    pv, pl = oracle.partials_extra(b.q, x.q_extra, b.k_pool, x.k_extra_pool, b.v_pool, D, b.indices, b.indptr,
+                                   b.last_page_len, b.first_page_offset, scale, plan.pages_per_chunk,
+                                   plan.request_indices, plan.kv_tile_indices)
+    assert_close(v[:plan.num_chunks], l[:plan.num_chunks], pv, pl, f"partials ppc={plan.pages_per_chunk}")
+    ro, rl = oracle.attention_extra(b.q, x.q_extra, b.k_pool, x.k_extra_pool, b.v_pool, D, b.indices, b.indptr,
+                                    b.last_page_len, b.first_page_offset, scale)
+    assert_close(out, lse, ro, rl, "merged")
+    return plan
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("ps,seq,fpo,override", [(1, [300, 77, 0, 1], [0, 0, 0, 0], 64),
+                                                 (16, [500, 33, 16], [3, 0, 15], 4),
+                                                 (64, [700, 64, 1], [10, 0, 0], 3),
+                                                 (5, [123, 40], [4, 2], 7)])
+def test_mla_shape_parity(dtype, ps, seq, fpo, override):
+    _check(_paged(seq, fpo, ps, 32, 1, dtype, seed=31 + ps), override=override)
+
+
+@pytest.mark.parametrize("G", [4, 16, 20])
+def test_group_sizes_and_kv_heads(G):
+    """Partial last q-group (G = 20: 16 + 4 heads) and two KV heads."""
+    _check(_paged([200, 95], [0, 1], 16, 2 * G, 2, torch.bfloat16, seed=40 + G), override=5)
+
+
+def test_separate_values_and_row_strides():
+    x = _paged([180, 40], [2, 0], 16, 16, 1, torch.float16, seed=50, k_width=520, v_width=528, shared_v=False)
+    _check(x, override=4)
+
+
+def test_plan_default_target_and_empty_requests():
+    _check(_paged([0, 1500, 0, 9], [0, 0, 0, 5], 16, 64, 1, torch.bfloat16, seed=60))
+
+
+def test_dsa_shaped_workload():
+    x = W.dsa_sparse_decode(batch=2, kv_len=4096, topk=2048)
+    _check(x, scale=x.batch.scale)
+
+
+def test_head_dim_512_plans_are_refused_by_the_single_stream_kernel():
+    x = _paged([64], [0], 16, 16, 1, torch.float16, seed=70)
+    b = x.batch
+    plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 16, 16, 1, D, pa.PA_F16, 8, 0, b.seq_lens)
+    d = x.to("cuda").batch
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_v2_decode_partial(plan, d.q, d.k_pool[..., :D].contiguous(), d.k_pool[..., :D].contiguous(), d.indices,
+                                d.indptr, d.last_page_len, d.first_page_offset, 0.1)
+    assert e.value.status == pa.PA_EUNSUPPORTED
