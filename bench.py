@@ -59,7 +59,7 @@ def parse_args():
     ap.add_argument("--context", type=int, default=32768)
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix",
-                             "tiny_csr", "block_sparse_selection", "crossover"],
+                             "tiny_csr", "block_sparse_selection", "crossover", "dsa_sparse_decode"],
                     help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
                          "(cold L2 for every step)")
     ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
@@ -906,10 +906,77 @@ def run_crossover(args):
     print(json.dumps(line), flush=True)
 
 
+def run_dsa(args):
+    """DSA-shaped decode with the second K stream (sparse-paged-decode.md, the DSA paragraphs): 128 query
+    heads over one latent KV head, latent 512 + rope 64 per row (the K buffer is 640 wide:
+    concat(kv_latent, indexer_key)), values = latent rows, 2048 selected rows per request (token-exact,
+    page_size 1).  Batch 1 (the pages' single-sequence case) and batch 16.  Each step is
+    pa_v2_decode_partial_extra + pa_merge_states from a CUDA graph after a 512 MiB L2 flush."""
+    from paged_attention_decode_gb300 import build as pa_build
+    from paged_attention_decode_gb300 import pa_v2 as pa
+    from paged_attention_decode_gb300 import workloads as W
+    import oracle
+
+    pa_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    cells = []
+    for B in (1, 16):
+        x = W.dsa_sparse_decode(batch=B)
+        b = x.batch
+        d = x.to(dev)
+        db = d.batch
+        dt = pa.KV_DTYPES[b.dtype]
+        plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, b.num_qo_heads, 1, x.dim, dt,
+                             pa.pa_v2_default_target_ctas(b.num_qo_heads, 1, x.dim, 1, dt), 0, b.seq_lens)
+        out = torch.empty(B, b.num_qo_heads, x.dim, device=dev)
+        lse = torch.empty(B, b.num_qo_heads, device=dev)
+        ws = (torch.empty(max(1, plan.num_chunks), b.num_qo_heads, x.dim, device=dev),
+              torch.empty(max(1, plan.num_chunks), b.num_qo_heads, device=dev))
+
+        def step():
+            pa.decode_extra(plan, db.q, d.q_extra, db.k_pool, db.v_pool, d.k_extra_pool, db.indices, db.indptr,
+                            db.last_page_len, db.first_page_offset, b.scale, out, lse, ws, None, stream)
+
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        r0 = slice(0, 1)
+        ref_o, _ = oracle.attention_extra(b.q[r0], x.q_extra[r0], b.k_pool, x.k_extra_pool, b.v_pool, x.dim,
+                                          b.indices[:b.seq_lens[0]], b.indptr[:2], b.last_page_len[r0],
+                                          b.first_page_offset[r0], b.scale)
+        err = float(abs(out[r0].cpu().double().numpy() - ref_o).max())
+        if not err <= 2e-3:
+            raise SystemExit(f"bench: dsa output disagrees with the oracle ({err:.3e}); refusing to time")
+        med, p10, p90 = _time_cold(step, stream, flush, args.warmup, args.steps, args.graph)
+        rows = sum(b.seq_lens)
+        nbytes = rows * (x.dim + x.q_extra.shape[-1]) * b.k_pool.element_size()
+        flops = 2.0 * rows * b.num_qo_heads * (x.dim + x.q_extra.shape[-1] + x.dim)
+        cells.append({"batch": B, "selected_rows_per_request": b.seq_lens[0], "chunks": plan.num_chunks,
+                      "ctas": plan.total_ctas, "us_per_step_median": med, "us_p10": p10, "us_p90": p90,
+                      "kv_bytes_per_step": nbytes, "kv_read_gbs": nbytes / (med * 1e-6) / 1e9,
+                      "flops_per_step": flops, "tflops": flops / (med * 1e-6) / 1e12})
+        del x, d, db
+        torch.cuda.empty_cache()
+    line = {"metric": "DSA decode us/step (median, cold L2), KV-read GB/s and TFLOP/s", "unit": "us/step",
+            "value": cells[0]["us_per_step_median"], "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "dsa_sparse_decode", "num_qo_heads": 128, "num_kv_heads": 1, "dim": 512,
+                       "extra_dim": 64, "row_stride": 640, "kv_dtype": "bfloat16", "page_size": 1,
+                       "kernel": "pa_v2_partial_extra_kernel (CUDA cores) + pa_merge_states",
+                       "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
+            "cells": cells}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "dsa_sparse_decode":
+        run_dsa(args)
     elif args.workload == "crossover":
         run_crossover(args)
     elif args.workload == "block_sparse_selection":

@@ -36,9 +36,9 @@ __device__ __forceinline__ float merge_weight(float l, float m) {
   return l == -INFINITY ? 0.f : fast_exp2(l - m);
 }
 
-// VECTOR: head_dim % 4 == 0 and head_dim <= 128 (one float4 per lane); else a
-// scalar loop over head_dim.
-template <bool VECTOR>
+// NV > 0: head_dim % 4 == 0 and head_dim <= 128 * NV (NV float4 per lane:
+// 1 up to head_dim 128, 4 up to 512); NV == 0: a scalar loop over head_dim.
+template <int NV>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     pa_merge_states_kernel(const float* __restrict__ v_in, const float* __restrict__ lse_in,
                            const int32_t* __restrict__ o_indptr, int32_t num_rows_out, int32_t num_partials,
@@ -46,7 +46,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                            float* __restrict__ lse_out, int32_t* status) {
   __shared__ float red[kMergeWarps];
   __shared__ float wsum_s[kMergeWarps];
-  __shared__ __align__(16) float acc_s[kMergeWarps][128];
+  constexpr bool VECTOR = NV > 0;
+  constexpr int U = NV > 1 ? kMergeUnroll / 2 : kMergeUnroll;  // rows in flight per warp
+  __shared__ __align__(16) float acc_s[kMergeWarps][VECTOR ? 128 * NV : 4];
 
   // the kernel that follows (normally the next step's partial kernel) may be
   // scheduled now; it waits for this grid to finish
@@ -70,41 +72,54 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   float* out = v_out + ((size_t)r * num_heads + h) * head_dim;
   if (VECTOR) {
     const int d4n = head_dim >> 2;
-    const bool active = lane < d4n;
     float m = -INFINITY, ws = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = i0 + warp; base < i1; base += kMergeWarps * kMergeUnroll) {
-      float l[kMergeUnroll];
-      float4 v[kMergeUnroll];
+    float4 acc[NV > 0 ? NV : 1];
 #pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
+    for (int k = 0; k < NV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = i0 + warp; base < i1; base += kMergeWarps * U) {
+      float l[U];
+      float4 v[U][NV > 0 ? NV : 1];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
         const int i = base + u * kMergeWarps;
         l[u] = i < i1 ? lse_in[i * hs + h] : -INFINITY;
-        v[u] = (i < i1 && active) ? reinterpret_cast<const float4*>(v_in + (i * hs + h) * head_dim)[lane]
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          const int q4 = lane + 32 * k;
+          v[u][k] = (i < i1 && q4 < d4n) ? reinterpret_cast<const float4*>(v_in + (i * hs + h) * head_dim)[q4]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
       float mb = m;
 #pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) mb = fmaxf(mb, l[u]);
+      for (int u = 0; u < U; ++u) mb = fmaxf(mb, l[u]);
       if (mb == -INFINITY) continue;
       const float sc = merge_weight(m, mb);  // 0 while nothing has been summed
       ws *= sc;
-      acc.x *= sc;
-      acc.y *= sc;
-      acc.z *= sc;
-      acc.w *= sc;
 #pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
+      for (int k = 0; k < NV; ++k) {
+        acc[k].x *= sc;
+        acc[k].y *= sc;
+        acc[k].z *= sc;
+        acc[k].w *= sc;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
         const float w = merge_weight(l[u], mb);
         ws += w;
-        acc.x = fmaf(w, v[u].x, acc.x);
-        acc.y = fmaf(w, v[u].y, acc.y);
-        acc.z = fmaf(w, v[u].z, acc.z);
-        acc.w = fmaf(w, v[u].w, acc.w);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          acc[k].x = fmaf(w, v[u][k].x, acc[k].x);
+          acc[k].y = fmaf(w, v[u][k].y, acc[k].y);
+          acc[k].z = fmaf(w, v[u][k].z, acc[k].z);
+          acc[k].w = fmaf(w, v[u][k].w, acc[k].w);
+        }
       }
       m = mb;
     }
-    if (active) reinterpret_cast<float4*>(acc_s[warp])[lane] = acc;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (lane + 32 * k < d4n) reinterpret_cast<float4*>(acc_s[warp])[lane + 32 * k] = acc[k];
     if (lane == 0) {
       red[warp] = m;
       wsum_s[warp] = ws;
@@ -171,7 +186,8 @@ extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, co
   if (num_rows_out < 0 || num_partials < 0 || num_heads < 1 || head_dim < 1) return PA_EINVAL;
   if (num_rows_out == 0) return PA_OK;
   if (!o_indptr || !v_out || !lse2_out || (num_partials > 0 && (!v_in || !lse2_in))) return PA_EINVAL;
-  const bool vec = head_dim % 4 == 0 && head_dim <= 128;
+  const int nv = head_dim % 4 != 0 ? 0 : head_dim <= 128 ? 1 : head_dim <= 512 ? 4 : 0;
+  const bool vec = nv > 0;
   if (vec && (((uintptr_t)v_in | (uintptr_t)v_out) & 15u)) return PA_EINVAL;
   const long long blocks = (long long)num_rows_out * num_heads;
   if (blocks > 0x7fffffffLL) return PA_EUNSUPPORTED;
@@ -188,10 +204,9 @@ extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t rc = vec ? cudaLaunchKernelEx(&cfg, pa::pa_merge_states_kernel<true>, v_in, lse2_in, o_indptr,
-                                            num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out, status)
-                       : cudaLaunchKernelEx(&cfg, pa::pa_merge_states_kernel<false>, v_in, lse2_in, o_indptr,
-                                            num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out,
-                                            status);
+  auto fn = nv == 1 ? pa::pa_merge_states_kernel<1> : nv == 4 ? pa::pa_merge_states_kernel<4>
+                                                              : pa::pa_merge_states_kernel<0>;
+  cudaError_t rc = cudaLaunchKernelEx(&cfg, fn, v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads,
+                                      head_dim, v_out, lse2_out, status);
   return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
 }

@@ -265,7 +265,7 @@ def test_plan_reuse_across_steps():
 # the merge kernel on its own
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("D", [64, 128, 6])
+@pytest.mark.parametrize("D", [64, 128, 6, 96, 256, 512, 200, 516])
 def test_merge_states_alone(D):
     rng = np.random.default_rng(D)
     groups = [1, 3, 0, 5, 2, 1, 7]
