@@ -929,8 +929,17 @@ def run_dsa(args):
         d = x.to(dev)
         db = d.batch
         dt = pa.KV_DTYPES[b.dtype]
+        wave = pa.pa_v2_default_target_ctas(b.num_qo_heads, 1, x.dim, 1, dt)
         plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, b.num_qo_heads, 1, x.dim, dt,
-                             pa.pa_v2_default_target_ctas(b.num_qo_heads, 1, x.dim, 1, dt), 0, b.seq_lens)
+                             wave, 0, b.seq_lens)
+        # the smallest chunk size whose CTAs fit one wave (the binary-search default can spill a few CTAs
+        # into a second wave)
+        from paged_attention_decode_gb300 import cascade as C
+        per = plan.q_groups * plan.num_kv_heads
+        fit = C.fit_pages_per_chunk([int(n) for n in b.seq_lens], per, wave)
+        if fit != plan.pages_per_chunk:
+            plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, b.num_qo_heads, 1, x.dim, dt,
+                                 wave, fit, b.seq_lens)
         out = torch.empty(B, b.num_qo_heads, x.dim, device=dev)
         lse = torch.empty(B, b.num_qo_heads, device=dev)
         ws = (torch.empty(max(1, plan.num_chunks), b.num_qo_heads, x.dim, device=dev),
@@ -965,7 +974,8 @@ def run_dsa(args):
             "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "dsa_sparse_decode", "num_qo_heads": 128, "num_kv_heads": 1, "dim": 512,
                        "extra_dim": 64, "row_stride": 640, "kv_dtype": "bfloat16", "page_size": 1,
-                       "kernel": "pa_v2_partial_extra_kernel (CUDA cores) + pa_merge_states",
+                       "kernel": "pa_v2_partial_extra_tc_kernel + pa_merge_states",
+                       "chunking": "smallest pages_per_chunk whose CTAs fit one wave",
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "cells": cells}
     print(json.dumps(line), flush=True)

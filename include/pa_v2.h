@@ -118,7 +118,7 @@ typedef struct pa_v2_plan_t {
 
 /* Query heads one CTA serves for GQA group size `group_size`: up to 16 for
  * f16/bf16 pools (tensor-core kernel), up to 8 for f32 pools (CUDA-core
- * kernel); head_dim 512 (the second-K-stream kernel, f16/bf16) up to 16.  The
+ * kernel); head_dim 512 (the second-K-stream kernels, f16/bf16) up to 8.  The
  * plan and the launcher both call this, so the CTA count and the grid cannot
  * drift apart (PR #984, What changed 2).  Returns 0 for an unsupported shape. */
 int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype);
@@ -260,8 +260,10 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
  * Row strides (RowStride) may exceed the dims read: the DSA K buffer holds
  * concat(kv_latent, indexer_key) per row and only the latent part is a key.
  * For MLA the values are the latent rows: pass v_pool == k_pool with the same
- * stride and each row is read once.  CUDA-core kernel (f32 arithmetic).
- *   plan        from pa_v2_plan with head_dim = Dim = 512 (16 query heads per
+ * stride and each row is read once.  Tensor cores (m16n8k16, q and P as
+ * hi + lo 16-bit halves, f32 accumulate); plan->kernel == 1 selects a
+ * CUDA-core variant (f32 arithmetic).
+ *   plan        from pa_v2_plan with head_dim = Dim = 512 (8 query heads per
  *               CTA, pa_v2_q_heads_per_cta); stack_members and out_row_step 1.
  *   q [batch, num_qo_heads, 512] f32 (16-byte aligned), q_extra [batch,
  *   num_qo_heads, 64] f32 (8-byte aligned).

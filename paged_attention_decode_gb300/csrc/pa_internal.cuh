@@ -389,8 +389,13 @@ int occupancy_partial_simt(int kv_dtype, int head_dim, int hpc, int* blocks_per_
 int launch_partial_tc(const LaunchArgs& a, bool use_tma);
 int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int* blocks_per_sm);
 
-// Second-K-stream kernel (head_dim 512 + extra 64; f16 / bf16 pools).
+// Second-K-stream kernels (head_dim 512 + extra 64; f16 / bf16 pools): CUDA
+// cores (pa_partial_extra.cu) and tensor cores (pa_partial_extra_tc.cu).
 int occupancy_partial_extra(int kv_dtype, int* blocks_per_sm);
+int occupancy_partial_extra_tc(int kv_dtype, int* blocks_per_sm);
+int launch_partial_extra_tc(const PartialParams& p, const void* q_extra, const void* k_extra, int64_t k_stride,
+                            int64_t v_stride, int64_t e_stride, bool shared_v, int kv_dtype, dim3 grid,
+                            cudaStream_t stream);
 
 // True when the tensor-core kernel stages this page size with TMA.
 inline bool tc_uses_tma(int page_size) {

@@ -15,16 +15,18 @@
 // entry (fpo + i) % ps; one CTA per (chunk, kv head, q-head group).
 //
 // Shapes served: Dim 512, ExtraDim 64 (DeepSeek's kv_lora_rank and
-// qk_rope_head_dim), up to 16 query heads per CTA, f16 / bf16 pools.
+// qk_rope_head_dim), up to 8 query heads per CTA, f16 / bf16 pools.  The
+// tensor-core variant (pa_partial_extra_tc.cu) is the default; this one runs
+// when plan.kernel == 1.
 //
-// Layout: 4 warps, each owning 4 of the CTA's query heads; all four read the
+// Layout: 4 warps, each owning 2 of the CTA's query heads; all four read the
 // same K / V rows (the later ones from L1).  Lane l owns latent dims
 // 16l .. 16l+15 (two 16-byte loads per row) and extra dims 2l, 2l+1, with the
 // matching query values (f32, scale * log2(e) folded in) in registers.  Two
 // tokens are scored per iteration (independent loads and shuffle trees), the
 // dot products reduced across lanes with butterfly shuffles, the online
 // softmax kept in f32 in every lane, and the output accumulated in the lane's
-// 16 dims x 4 heads.  No shared memory, no barriers.
+// 16 dims x 2 heads.  No shared memory, no barriers.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,8 +44,8 @@ namespace {
 constexpr int kXDim = 512;        // Dim
 constexpr int kXExtra = 64;       // ExtraDim
 constexpr int kXWarps = 4;
-constexpr int kXHeadsPerWarp = 4;
-constexpr int kXHeads = kXWarps * kXHeadsPerWarp;  // 16 query heads per CTA
+constexpr int kXHeadsPerWarp = 2;
+constexpr int kXHeads = kXWarps * kXHeadsPerWarp;  // 8 query heads per CTA
 constexpr int kXTok = 2;          // tokens per iteration
 constexpr int kXLaneDims = kXDim / 32;             // 16 latent dims per lane
 constexpr int kXLaneExtra = kXExtra / 32;          // 2 extra dims per lane
@@ -69,7 +71,7 @@ template <> struct XT<__nv_bfloat16> {
 };
 
 template <typename T, bool SHARED_V>
-__global__ void __launch_bounds__(kXWarps * 32)
+__global__ void __launch_bounds__(kXWarps * 32, 4)
     pa_v2_partial_extra_kernel(const PartialParams p, const ExtraFields x) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -313,6 +315,7 @@ extern "C" pa_status pa_v2_decode_partial_extra(
   const bool shared_v = v_pool == k_pool && v_row_stride == k_row_stride;
   ExtraInstance inst;
   if (!extra_pick(kv_dtype, shared_v, &inst)) return PA_EUNSUPPORTED;
+  const bool tc = plan->kernel != 1;
 
   PartialParams p;
   std::memset(&p, 0, sizeof(p));
@@ -352,6 +355,10 @@ extern "C" pa_status pa_v2_decode_partial_extra(
   x.e_stride = k_extra_row_stride;
 
   const dim3 grid((unsigned)plan->num_chunks, (unsigned)(plan->num_kv_heads * plan->q_groups));
+  if (tc)
+    return (pa_status)launch_partial_extra_tc(p, q_extra, k_extra_pool, k_row_stride, v_row_stride,
+                                              k_extra_row_stride, shared_v, kv_dtype, grid,
+                                              static_cast<cudaStream_t>(cuda_stream));
   const cudaError_t rc =
       launch_dependent(inst.fn, grid, dim3(kXWarps * 32), 0, static_cast<cudaStream_t>(cuda_stream), p, x);
   return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;

@@ -31,12 +31,13 @@ def _paged(seq, fpo, ps, Hq, Hkv, dtype, seed, k_width=640, v_width=None, shared
     return W.ExtraStreamBatch(b, qe, ke, D, shared_v)
 
 
-def _check(x, target=None, override=0, scale=None):
+def _check(x, target=None, override=0, scale=None, kernel=0):
     b = x.batch
     dt = pa.KV_DTYPES[b.dtype]
     tgt = target or pa.pa_v2_default_target_ctas(b.num_qo_heads, b.num_kv_heads, D, b.page_size, dt)
     plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
                          b.num_kv_heads, D, dt, tgt, override, b.seq_lens)
+    plan.struct.kernel = kernel                       # 0: tensor cores, 1: CUDA cores
     scale = scale or 1.0 / math.sqrt(D + E)
     d = x.to("cuda")
     db = d.batch
@@ -57,13 +58,14 @@ def _check(x, target=None, override=0, scale=None):
     return plan
 
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("ps,seq,fpo,override", [(1, [300, 77, 0, 1], [0, 0, 0, 0], 64),
                                                  (16, [500, 33, 16], [3, 0, 15], 4),
                                                  (64, [700, 64, 1], [10, 0, 0], 3),
                                                  (5, [123, 40], [4, 2], 7)])
-def test_mla_shape_parity(dtype, ps, seq, fpo, override):
-    _check(_paged(seq, fpo, ps, 32, 1, dtype, seed=31 + ps), override=override)
+def test_mla_shape_parity(dtype, ps, seq, fpo, override, kernel):
+    _check(_paged(seq, fpo, ps, 32, 1, dtype, seed=31 + ps), override=override, kernel=kernel)
 
 
 @pytest.mark.parametrize("G", [4, 16, 20])
@@ -72,18 +74,20 @@ def test_group_sizes_and_kv_heads(G):
     _check(_paged([200, 95], [0, 1], 16, 2 * G, 2, torch.bfloat16, seed=40 + G), override=5)
 
 
-def test_separate_values_and_row_strides():
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_separate_values_and_row_strides(kernel):
     x = _paged([180, 40], [2, 0], 16, 16, 1, torch.float16, seed=50, k_width=520, v_width=528, shared_v=False)
-    _check(x, override=4)
+    _check(x, override=4, kernel=kernel)
 
 
 def test_plan_default_target_and_empty_requests():
     _check(_paged([0, 1500, 0, 9], [0, 0, 0, 5], 16, 64, 1, torch.bfloat16, seed=60))
 
 
-def test_dsa_shaped_workload():
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_dsa_shaped_workload(kernel):
     x = W.dsa_sparse_decode(batch=2, kv_len=4096, topk=2048)
-    _check(x, scale=x.batch.scale)
+    _check(x, scale=x.batch.scale, kernel=kernel)
 
 
 def test_head_dim_512_plans_are_refused_by_the_single_stream_kernel():
