@@ -69,6 +69,7 @@ def parse_args():
                     help="time the one-launch pa_v2_decode (merge fused into the partial kernel) instead of "
                          "pa_v2_decode_partial + pa_merge_states")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
+    ap.add_argument("--dsa-batch", default="1,16", help="dsa_sparse_decode: comma-separated batch sizes")
     ap.add_argument("--profile", type=int, default=0,
                     help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
     return ap.parse_args()
@@ -923,7 +924,7 @@ def run_dsa(args):
     stream = torch.cuda.Stream(device=dev)
     flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
     cells = []
-    for B in (1, 16):
+    for B in [int(v) for v in args.dsa_batch.split(",")]:
         x = W.dsa_sparse_decode(batch=B)
         b = x.batch
         d = x.to(dev)
@@ -949,6 +950,14 @@ def run_dsa(args):
             pa.decode_extra(plan, db.q, d.q_extra, db.k_pool, db.v_pool, d.k_extra_pool, db.indices, db.indptr,
                             db.last_page_len, db.first_page_offset, b.scale, out, lse, ws, None, stream)
 
+        if args.profile:
+            with torch.cuda.stream(stream):
+                for _ in range(args.profile):
+                    step()
+            stream.synchronize()
+            print(f"profile mode: dsa batch {B}, {args.profile} steps, {plan.total_ctas} CTAs", flush=True)
+            continue
+
         with torch.cuda.stream(stream):
             step()
         stream.synchronize()
@@ -969,6 +978,19 @@ def run_dsa(args):
                       "flops_per_step": flops, "tflops": flops / (med * 1e-6) / 1e12})
         del x, d, db
         torch.cuda.empty_cache()
+    if args.profile:
+        return
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak, tkind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        tpeak, tkind = 1900.0, "fallback"
+    big = cells[-1]
+    roofline = {"bound": "tensor", "achieved": big["tflops"], "peak": tpeak, "unit": "TFLOP/s",
+                "frac": big["tflops"] / tpeak, "traffic": None, "cell": f"batch {big['batch']}",
+                "peak_source": tkind,
+                "note": "useful flops (QK over 576 dims + PV over 512, per head and row) over the step time; "
+                        "the MMAs issued are twice that (q and P as hi + lo halves)"}
     line = {"metric": "DSA decode us/step (median, cold L2), KV-read GB/s and TFLOP/s", "unit": "us/step",
             "value": cells[0]["us_per_step_median"], "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
@@ -977,7 +999,7 @@ def run_dsa(args):
                        "kernel": "pa_v2_partial_extra_tc_kernel + pa_merge_states",
                        "chunking": "smallest pages_per_chunk whose CTAs fit one wave",
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
-            "cells": cells}
+            "cells": cells, "roofline": roofline}
     print(json.dumps(line), flush=True)
 
 
