@@ -174,6 +174,10 @@ int32_t pa_v2_plan_matches(const pa_v2_plan_t* plan, const int32_t* indptr,
  * Alignment: pools, q, v_out 16-byte aligned.  num_pages: pool pages
  * (num_pages * page_size < 2^31).  num_indices: length of `indices`.
  * status: nullable device int32 receiving PA_DEVICE_* bits.
+ * A one-request plan (batch 1) given num_indices == plan->num_indices fixes
+ * chunk c to tile c of request 0 over page slots 0 .. num_indices-1, so the
+ * kernel reads neither request_indices / kv_tile_indices nor indptr (they
+ * must still be the plan's; pa_v2_plan_matches checks a host indptr).
  * Supported: head_dim 64 or 128; kv_dtype f32, f16, bf16; page_size 1..16 or
  * a multiple of 16 up to 256 (head_dim 512 plans: pa_v2_decode_partial_extra). */
 pa_status pa_v2_decode_partial(const pa_v2_plan_t* plan, const float* q, const void* k_pool,

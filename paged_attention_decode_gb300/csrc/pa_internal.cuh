@@ -46,6 +46,7 @@ struct PartialParams {
   const int32_t* out_rows;     // final output row of request r (member m when stacked), or null
   int64_t num_pages;
   int64_t num_indices;
+  int32_t single_pages;  // > 0: a one-request plan of this many pages (chunk c is tile c of request 0)
   int32_t batch;
   int32_t num_qo_heads;
   int32_t num_kv_heads;
@@ -125,19 +126,27 @@ struct StageGeom {
 // floor(16 / ps) whole pages when ps <= 16, else one 16-row slice of a page.
 __device__ __forceinline__ ChunkGeom chunk_geom(const PartialParams& p, int c, int* r_out) {
   ChunkGeom g;
-  int r = p.request_indices[c];
-  const int tile = p.kv_tile_indices[c];
+  int r = 0, tile = c;
   bool bad = false;
-  if (r < 0 || r >= p.batch) {
-    if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_REQUEST);
-    bad = true;
-    r = 0;
-  }
-  g.slot_base = p.indptr[r];
-  g.pages = p.indptr[r + 1] - g.slot_base;
-  if (!bad && (g.slot_base < 0 || g.pages < 0 || (int64_t)g.slot_base + g.pages > p.num_indices)) {
-    if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_SLOT);
-    bad = true;
+  if (p.single_pages > 0) {
+    // one request: its page slots are 0 .. single_pages-1 (indptr = [0, num_indices] of the plan), and
+    // chunk c is its tile c -- no chunk-array or indptr load stands before the first page-id load
+    g.slot_base = 0;
+    g.pages = p.single_pages;
+  } else {
+    r = p.request_indices[c];
+    tile = p.kv_tile_indices[c];
+    if (r < 0 || r >= p.batch) {
+      if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_REQUEST);
+      bad = true;
+      r = 0;
+    }
+    g.slot_base = p.indptr[r];
+    g.pages = p.indptr[r + 1] - g.slot_base;
+    if (!bad && (g.slot_base < 0 || g.pages < 0 || (int64_t)g.slot_base + g.pages > p.num_indices)) {
+      if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_SLOT);
+      bad = true;
+    }
   }
   g.fpo = p.first_page_offset[r];
   g.lpl = p.last_page_len[r];

@@ -202,6 +202,9 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
   }
   p.num_pages = num_pages;
   p.num_indices = num_indices;
+  // a one-request plan fixes chunk c to tile c of request 0 and that request's slots to 0 .. num_indices-1
+  if (plan->batch == 1 && num_indices == plan->num_indices && num_indices > 0 && num_indices <= INT32_MAX)
+    p.single_pages = (int32_t)num_indices;
   p.batch = plan->batch;
   p.num_qo_heads = plan->num_qo_heads;
   p.num_kv_heads = plan->num_kv_heads;

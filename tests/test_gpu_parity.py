@@ -337,7 +337,8 @@ def test_bad_o_indptr_is_reported():
 
 
 def test_out_of_range_request_index_is_reported():
-    b = W.make_batch("badreq", [300], [0], 16, 8, 2, 128, torch.float16, seed=18)
+    # two requests: a one-request plan fixes every chunk's request and reads no chunk arrays
+    b = W.make_batch("badreq", [300, 40], [0, 0], 16, 8, 2, 128, torch.float16, seed=18)
     plan = make_plan(b, target=16)
     d = b.to("cuda")
     ri, ti, _ = plan.device_arrays("cuda")
