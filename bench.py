@@ -62,7 +62,9 @@ def parse_args():
                              "tiny_csr", "block_sparse_selection", "crossover", "dsa_sparse_decode"],
                     help="the 32K Llama-3-8B decode is the headline; the others print a per-step line "
                          "(cold L2 for every step)")
-    ap.add_argument("--kernel", type=int, default=0, help="plan.kernel: 0 default, 1 CUDA-core partial kernel")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="plan.kernel: 0 default, 1 CUDA-core partial kernel, 2 (dsa_sparse_decode) the "
+                         "warp-level tensor-core second-K-stream kernel")
     ap.add_argument("--tune", action="store_true",
                     help="--workload runs: also time the chunk size picked by the autotuner")
     ap.add_argument("--fused", action="store_true",
@@ -109,6 +111,7 @@ def measured_peak():
 KERNEL_SOURCES = {
     "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_internal.cuh", "pa_device.cuh", "pa_mma.cuh"],
     "pa_v2_partial_simt_kernel": ["pa_partial_simt.cu", "pa_internal.cuh", "pa_device.cuh"],
+    "pa_v2_partial_extra_tc05_kernel": ["pa_partial_extra_tc05.cu", "pa_internal.cuh", "pa_device.cuh", "pa_mma.cuh"],
 }
 
 
@@ -120,10 +123,10 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()
 
 
-def ncu_traffic(kernel: str):
-    """Per-launch DRAM bytes (read + write) from the committed ncu summary of `kernel` on this workload,
+def ncu_traffic(kernel: str, workload: str = "llama3_8b_32k"):
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary of `kernel` on `workload`,
     or None when the kernel's sources changed since the capture."""
-    path = os.path.join(ROOT, "profiles", f"{kernel.replace('pa_v2_', '')}_llama3_8b_32k.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel.replace('pa_v2_', '')}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -934,13 +937,16 @@ def run_dsa(args):
         plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, b.num_qo_heads, 1, x.dim, dt,
                              wave, 0, b.seq_lens)
         # the smallest chunk size whose CTAs fit one wave (the binary-search default can spill a few CTAs
-        # into a second wave)
+        # into a second wave), rounded up to whole 128-row tiles of the tensor-memory kernel (a partial
+        # tile costs the MMAs of a full one)
         from paged_attention_decode_gb300 import cascade as C
         per = plan.q_groups * plan.num_kv_heads
         fit = C.fit_pages_per_chunk([int(n) for n in b.seq_lens], per, wave)
+        fit = min(-(-fit // 128) * 128, max(int(n) for n in b.seq_lens))
         if fit != plan.pages_per_chunk:
             plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, b.num_qo_heads, 1, x.dim, dt,
                                  wave, fit, b.seq_lens)
+        plan.struct.kernel = args.kernel
         out = torch.empty(B, b.num_qo_heads, x.dim, device=dev)
         lse = torch.empty(B, b.num_qo_heads, device=dev)
         ws = (torch.empty(max(1, plan.num_chunks), b.num_qo_heads, x.dim, device=dev),
@@ -987,7 +993,10 @@ def run_dsa(args):
         tpeak, tkind = 1900.0, "fallback"
     big = cells[-1]
     roofline = {"bound": "tensor", "achieved": big["tflops"], "peak": tpeak, "unit": "TFLOP/s",
-                "frac": big["tflops"] / tpeak, "traffic": None, "cell": f"batch {big['batch']}",
+                "frac": big["tflops"] / tpeak,
+                "traffic": ncu_traffic("pa_v2_partial_extra_tc05_kernel", "dsa_b16")
+                if big["batch"] == 16 and args.kernel == 0 else None,
+                "cell": f"batch {big['batch']}",
                 "peak_source": tkind,
                 "note": "useful flops (QK over 576 dims + PV over 512, per head and row) over the step time; "
                         "the MMAs issued are twice that (q and P as hi + lo halves)"}
@@ -996,8 +1005,9 @@ def run_dsa(args):
             "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "dsa_sparse_decode", "num_qo_heads": 128, "num_kv_heads": 1, "dim": 512,
                        "extra_dim": 64, "row_stride": 640, "kv_dtype": "bfloat16", "page_size": 1,
-                       "kernel": "pa_v2_partial_extra_tc_kernel + pa_merge_states",
-                       "chunking": "smallest pages_per_chunk whose CTAs fit one wave",
+                       "kernel": ["pa_v2_partial_extra_tc05_kernel", "pa_v2_partial_extra_kernel",
+                                  "pa_v2_partial_extra_tc_kernel"][args.kernel] + " + pa_merge_states",
+                       "chunking": "smallest pages_per_chunk whose CTAs fit one wave, in whole 128-row tiles",
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "cells": cells, "roofline": roofline}
     print(json.dumps(line), flush=True)

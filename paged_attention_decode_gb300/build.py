@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["pa_plan.cpp", "pa_cascade.cpp", "pa_partial.cu", "pa_partial_simt.cu", "pa_partial_tc.cu", "pa_merge.cu",
            "pa_noalloc.cu", "pa_select.cu", "pa_host_step.cpp", "pa_partial_extra.cu",
-           "pa_partial_extra_tc.cu"]
+           "pa_partial_extra_tc.cu", "pa_partial_extra_tc05.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -405,6 +405,11 @@ int occupancy_partial_extra_tc(int kv_dtype, int* blocks_per_sm);
 int launch_partial_extra_tc(const PartialParams& p, const void* q_extra, const void* k_extra, int64_t k_stride,
                             int64_t v_stride, int64_t e_stride, bool shared_v, int kv_dtype, dim3 grid,
                             cudaStream_t stream);
+// The tensor-memory (tcgen05) second-K-stream kernel: values read from the key
+// tile, up to 32 query heads per CTA (p.hpc <= 32).
+int occupancy_partial_extra_tc05(int kv_dtype, int* blocks_per_sm);
+int launch_partial_extra_tc05(const PartialParams& p, const void* q_extra, const void* k_extra, int64_t k_stride,
+                              int64_t e_stride, int kv_dtype, dim3 grid, cudaStream_t stream);
 
 // True when the tensor-core kernel stages this page size with TMA.
 inline bool tc_uses_tma(int page_size) {

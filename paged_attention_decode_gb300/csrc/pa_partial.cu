@@ -91,7 +91,7 @@ bool use_tensor_cores(int kv_dtype, int kernel) {
 extern "C" int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype) {
   if (group_size < 1) return 0;
   if (head_dim == 512)  // the second-K-stream kernels (pa_v2_decode_partial_extra): f16 / bf16 only
-    return kv_dtype == PA_F16 || kv_dtype == PA_BF16 ? (group_size < 8 ? group_size : 8) : 0;
+    return kv_dtype == PA_F16 || kv_dtype == PA_BF16 ? (group_size < 32 ? group_size : 32) : 0;
   if (head_dim != 64 && head_dim != 128) return 0;
   if (kv_dtype == PA_F16 || kv_dtype == PA_BF16) return group_size < 16 ? group_size : 16;
   if (kv_dtype == PA_F32) return group_size < 8 ? group_size : 8;
@@ -111,7 +111,7 @@ extern "C" pa_status pa_v2_default_target_ctas(int32_t device, int32_t num_qo_he
   if (device != prev && cudaSetDevice(device) != cudaSuccess) return PA_ECUDA;
   int sms = 0, per_sm = 0, rc = PA_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess) {
-    rc = head_dim == 512 ? pa::occupancy_partial_extra_tc(kv_dtype, &per_sm)
+    rc = head_dim == 512 ? pa::occupancy_partial_extra_tc05(kv_dtype, &per_sm)
          : pa::use_tensor_cores(kv_dtype, 0)
              ? pa::occupancy_partial_tc(kv_dtype, head_dim, hpc, pa::tc_uses_tma(page_size), &per_sm)
              : pa::occupancy_partial_simt(kv_dtype, head_dim, hpc, &per_sm);

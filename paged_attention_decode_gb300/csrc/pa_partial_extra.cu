@@ -301,8 +301,8 @@ extern "C" pa_status pa_v2_decode_partial_extra(
       !first_page_offset || !request_indices || !kv_tile_indices || !v_out || !lse2_out)
     return PA_EINVAL;
   const int G = plan->num_qo_heads / plan->num_kv_heads;
-  if (plan->q_heads_per_cta != pa_v2_q_heads_per_cta(G, kXDim, kv_dtype) || plan->q_heads_per_cta > kXHeads ||
-      plan->stack_members != 1 || plan->out_row_step != 1)
+  if (plan->q_heads_per_cta != pa_v2_q_heads_per_cta(G, kXDim, kv_dtype) || plan->stack_members != 1 ||
+      plan->out_row_step != 1 || plan->kernel < 0 || plan->kernel > 2)
     return PA_EINVAL;
   // rows are read 16 bytes (extra rows 4 bytes) at a time from 16-byte-aligned row starts;
   // q and v_out are read / written as float4 and q_extra as float2
@@ -315,6 +315,9 @@ extern "C" pa_status pa_v2_decode_partial_extra(
   const bool shared_v = v_pool == k_pool && v_row_stride == k_row_stride;
   ExtraInstance inst;
   if (!extra_pick(kv_dtype, shared_v, &inst)) return PA_EUNSUPPORTED;
+  // plan->kernel 0: the tensor-memory kernel (values in the key tile) or, for separate values, the
+  // warp-level tensor-core kernel; 1: CUDA cores; 2: the warp-level tensor-core kernel
+  const bool tc05 = plan->kernel == 0 && shared_v;
   const bool tc = plan->kernel != 1;
 
   PartialParams p;
@@ -335,12 +338,19 @@ extern "C" pa_status pa_v2_decode_partial_extra(
   p.out_row_step = 1;
   p.num_pages = num_pages;
   p.num_indices = num_indices;
+  // a one-request plan fixes chunk c to tile c of request 0 and that request's slots to 0 .. num_indices-1
+  if (plan->batch == 1 && num_indices == plan->num_indices && num_indices > 0 && num_indices <= INT32_MAX)
+    p.single_pages = (int32_t)num_indices;
   p.batch = plan->batch;
   p.num_qo_heads = plan->num_qo_heads;
   p.num_kv_heads = plan->num_kv_heads;
   p.group = G;
   p.hpc = plan->q_heads_per_cta;
   p.q_groups = plan->q_groups;
+  if (!tc05) {  // the other kernels serve 8 query heads per CTA: regroup the plan's heads
+    p.hpc = G < kXHeads ? G : kXHeads;
+    p.q_groups = (G + p.hpc - 1) / p.hpc;
+  }
   p.page_size = plan->page_size;
   p.pages_per_chunk = plan->pages_per_chunk;
   const FastDiv fd = FastDiv::make((uint32_t)plan->page_size);
@@ -354,7 +364,10 @@ extern "C" pa_status pa_v2_decode_partial_extra(
   x.v_stride = v_row_stride;
   x.e_stride = k_extra_row_stride;
 
-  const dim3 grid((unsigned)plan->num_chunks, (unsigned)(plan->num_kv_heads * plan->q_groups));
+  const dim3 grid((unsigned)plan->num_chunks, (unsigned)(plan->num_kv_heads * p.q_groups));
+  if (tc05)
+    return (pa_status)launch_partial_extra_tc05(p, q_extra, k_extra_pool, k_row_stride, k_extra_row_stride,
+                                                kv_dtype, grid, static_cast<cudaStream_t>(cuda_stream));
   if (tc)
     return (pa_status)launch_partial_extra_tc(p, q_extra, k_extra_pool, k_row_stride, v_row_stride,
                                               k_extra_row_stride, shared_v, kv_dtype, grid,

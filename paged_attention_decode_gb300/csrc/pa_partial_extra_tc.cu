@@ -168,20 +168,39 @@ __global__ void __maxnreg__(224)
 
   // ---- Q^T tile (hi + lo halves) in shared memory, once per CTA ----
   {
+    // a thread's q loads are issued 12 at a time before its shared-memory stores, so they
+    // overlap instead of paying one memory latency each
     unsigned char* qhi = smem + L::QOFF;
     unsigned char* qlo = qhi + L::QHALF;
-    for (int idx = threadIdx.x; idx < kMHeads * (kMDim + kMExtra); idx += kMWarps * 32) {
-      const int h = idx / (kMDim + kMExtra);
-      const int d = idx - h * (kMDim + kMExtra);
-      float v = 0.f;
-      if (h < nheads) {
-        const size_t qrow = (size_t)r * p.num_qo_heads + h_first + h;
-        v = (d < kMDim ? p.q[qrow * kMDim + d] : x.q_extra[qrow * kMExtra + (d - kMDim)]) * p.scale_log2;
+    constexpr int kTotal = kMHeads * (kMDim + kMExtra);
+    constexpr int kBatch = 12;
+#pragma unroll 1
+    for (int base = 0; base < kTotal; base += kBatch * kMWarps * 32) {
+      float qv[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int idx = base + threadIdx.x + k * kMWarps * 32;
+        const int h = idx / (kMDim + kMExtra);
+        const int d = idx - h * (kMDim + kMExtra);
+        qv[k] = 0.f;
+        if (idx < kTotal && h < nheads) {
+          const size_t qrow = (size_t)r * p.num_qo_heads + h_first + h;
+          qv[k] = d < kMDim ? __ldg(p.q + qrow * kMDim + d) : __ldg(x.q_extra + qrow * kMExtra + (d - kMDim));
+        }
       }
-      const float hi = TC<T>::round(v);
-      const uint32_t off = qswz(h, d >> 3) + (d & 7) * 2;
-      *reinterpret_cast<unsigned short*>(qhi + off) = TC<T>::bits(hi);
-      *reinterpret_cast<unsigned short*>(qlo + off) = TC<T>::bits(v - hi);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int idx = base + threadIdx.x + k * kMWarps * 32;
+        if (idx < kTotal) {
+          const int h = idx / (kMDim + kMExtra);
+          const int d = idx - h * (kMDim + kMExtra);
+          const float v = qv[k] * p.scale_log2;
+          const float hi = TC<T>::round(v);
+          const uint32_t off = qswz(h, d >> 3) + (d & 7) * 2;
+          *reinterpret_cast<unsigned short*>(qhi + off) = TC<T>::bits(hi);
+          *reinterpret_cast<unsigned short*>(qlo + off) = TC<T>::bits(v - hi);
+        }
+      }
     }
   }
   __syncwarp();     // reconverge the per-thread branches before the aligned barrier

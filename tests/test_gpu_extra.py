@@ -1,6 +1,8 @@
-"""GPU: the second-K-stream partial kernel (pa_v2_decode_partial_extra) against the oracle -- partials
+"""GPU: the second-K-stream partial kernels (pa_v2_decode_partial_extra) against the oracle -- partials
 chunk by chunk and the merged result -- on MLA-shaped (values = latent rows) and separate-V inputs,
-token-exact and paged tables, f16 and bf16, and the DSA-shaped workload."""
+token-exact and paged tables, f16 and bf16, and the DSA-shaped workload.  plan.kernel 0 runs the
+tensor-memory kernel (values in the key tile; separate values fall back to the warp-level tensor-core
+kernel), 1 the CUDA-core kernel, 2 the warp-level tensor-core kernel."""
 import math
 
 import pytest
@@ -37,7 +39,7 @@ def _check(x, target=None, override=0, scale=None, kernel=0):
     tgt = target or pa.pa_v2_default_target_ctas(b.num_qo_heads, b.num_kv_heads, D, b.page_size, dt)
     plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
                          b.num_kv_heads, D, dt, tgt, override, b.seq_lens)
-    plan.struct.kernel = kernel                       # 0: tensor cores, 1: CUDA cores
+    plan.struct.kernel = kernel
     scale = scale or 1.0 / math.sqrt(D + E)
     d = x.to("cuda")
     db = d.batch
@@ -58,7 +60,7 @@ def _check(x, target=None, override=0, scale=None, kernel=0):
     return plan
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("ps,seq,fpo,override", [(1, [300, 77, 0, 1], [0, 0, 0, 0], 64),
                                                  (16, [500, 33, 16], [3, 0, 15], 4),
@@ -68,13 +70,38 @@ def test_mla_shape_parity(dtype, ps, seq, fpo, override, kernel):
     _check(_paged(seq, fpo, ps, 32, 1, dtype, seed=31 + ps), override=override, kernel=kernel)
 
 
-@pytest.mark.parametrize("G", [4, 16, 20])
-def test_group_sizes_and_kv_heads(G):
-    """Partial last q-group (G = 20: 16 + 4 heads) and two KV heads."""
-    _check(_paged([200, 95], [0, 1], 16, 2 * G, 2, torch.bfloat16, seed=40 + G), override=5)
+@pytest.mark.parametrize("kernel", [0, 2])
+@pytest.mark.parametrize("G", [4, 16, 20, 40])
+def test_group_sizes_and_kv_heads(G, kernel):
+    """Partial last q-groups (G = 20: 8 + 8 + 4 heads for the 8-head kernels; G = 40: 32 + 8 for the
+    tensor-memory kernel) and two KV heads."""
+    _check(_paged([200, 95], [0, 1], 16, 2 * G, 2, torch.bfloat16, seed=40 + G), override=5, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("ps,seq,fpo,override", [(1, [3000, 129, 128, 127], [0, 0, 0, 0], 1000),
+                                                 (256, [900, 300], [200, 0], 2),
+                                                 (16, [2100], [7], 80)])
+def test_multi_tile_chunks(dtype, ps, seq, fpo, override):
+    """Chunks of several 128-row tiles (the tensor-memory kernel's refill pipeline), tile-sized and
+    one-off-tile-sized requests, and a 256-row page whose first tile is all before first_page_offset."""
+    _check(_paged(seq, fpo, ps, 32, 1, dtype, seed=80 + ps), override=override)
+
+
+@pytest.mark.parametrize("kernel", [0, 2])
+def test_rising_scores_rescale_the_accumulator(kernel):
+    """Extra-key rows grow with their position (the values do not), so the tiles' maximum scores climb
+    by several times 8 (log2 units) along the chunk: the tensor-memory kernel raises its running
+    maxima and rescales O^T and the row sums in place, repeatedly."""
+    x = _paged([1400], [0], 1, 32, 1, torch.bfloat16, seed=90)
+    ke = x.k_extra_pool.float()
+    rows = x.batch.indices[:1400].long()         # page_size 1: token t is pool row indices[t]
+    ke[rows] *= (1.0 + torch.arange(1400, dtype=torch.float32) / 32.0).view(-1, 1, 1, 1)
+    x.k_extra_pool = ke.to(torch.bfloat16)
+    _check(x, override=1400, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 def test_separate_values_and_row_strides(kernel):
     x = _paged([180, 40], [2, 0], 16, 16, 1, torch.float16, seed=50, k_width=520, v_width=528, shared_v=False)
     _check(x, override=4, kernel=kernel)
@@ -84,7 +111,7 @@ def test_plan_default_target_and_empty_requests():
     _check(_paged([0, 1500, 0, 9], [0, 0, 0, 5], 16, 64, 1, torch.bfloat16, seed=60))
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 def test_dsa_shaped_workload(kernel):
     x = W.dsa_sparse_decode(batch=2, kv_len=4096, topk=2048)
     _check(x, scale=x.batch.scale, kernel=kernel)

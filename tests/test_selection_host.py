@@ -49,6 +49,6 @@ def test_device_status_bit_for_bad_blocks_maps_to_eoob():
 @pytest.mark.parametrize("G", [1, 4, 16, 20, 128])
 def test_heads_per_cta_rule_for_the_second_k_stream(G):
     for dt in (pa.PA_F16, pa.PA_BF16):
-        assert pa.pa_v2_q_heads_per_cta(G, 512, dt) == min(G, 8)
+        assert pa.pa_v2_q_heads_per_cta(G, 512, dt) == min(G, 32)
     assert pa.pa_v2_q_heads_per_cta(G, 512, pa.PA_F32) == 0
     assert pa.pa_v2_q_heads_per_cta(G, 256, pa.PA_F16) == 0
