@@ -97,8 +97,10 @@ typedef struct pa_v2_plan_t {
     int32_t needs_merge;              /* 1 iff num_chunks > batch */
     int32_t target_ctas, total_ctas;  /* total_ctas = num_chunks * num_kv_heads * q_groups */
     int32_t kernel;                   /* 0: tensor cores for f16/bf16 pools, CUDA cores for f32;
-                                         1: CUDA cores (needs q_heads_per_cta <= 8).  Set by the
-                                         caller after pa_v2_plan; pa_v2_plan writes 0. */
+                                         1: CUDA cores (needs q_heads_per_cta <= 8 for head_dim
+                                         64 / 128); 2 (head_dim 512 only): the warp-level
+                                         tensor-core kernel.  Set by the caller after pa_v2_plan;
+                                         pa_v2_plan writes 0. */
     int32_t stack_members;            /* Cascade level 0 (cascade-attention.md): when M > 1 the plan's
                                          single request holds the query heads of M members stacked
                                          h0 = kv*(M*Gm) + m*Gm + g (Gm = num_qo_heads / (M *
@@ -118,9 +120,10 @@ typedef struct pa_v2_plan_t {
 
 /* Query heads one CTA serves for GQA group size `group_size`: up to 16 for
  * f16/bf16 pools (tensor-core kernel), up to 8 for f32 pools (CUDA-core
- * kernel); head_dim 512 (the second-K-stream kernels, f16/bf16) up to 8.  The
- * plan and the launcher both call this, so the CTA count and the grid cannot
- * drift apart (PR #984, What changed 2).  Returns 0 for an unsupported shape. */
+ * kernel); head_dim 512 (the second-K-stream kernels, f16/bf16) up to 32, the
+ * tensor-memory kernel's N.  The plan and the launcher both call this, so the
+ * CTA count and the grid cannot drift apart (PR #984, What changed 2).
+ * Returns 0 for an unsupported shape. */
 int32_t pa_v2_q_heads_per_cta(int32_t group_size, int32_t head_dim, int32_t kv_dtype);
 
 /* Occupancy-derived CTA target for `device`: SM count times the partial
@@ -264,11 +267,20 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
  * Row strides (RowStride) may exceed the dims read: the DSA K buffer holds
  * concat(kv_latent, indexer_key) per row and only the latent part is a key.
  * For MLA the values are the latent rows: pass v_pool == k_pool with the same
- * stride and each row is read once.  Tensor cores (m16n8k16, q and P as
- * hi + lo 16-bit halves, f32 accumulate); plan->kernel == 1 selects a
- * CUDA-core variant (f32 arithmetic).
- *   plan        from pa_v2_plan with head_dim = Dim = 512 (8 query heads per
- *               CTA, pa_v2_q_heads_per_cta); stack_members and out_row_step 1.
+ * stride and each row is read once.  Kernels, by plan->kernel:
+ *   0 (default) values in the key tile (v_pool == k_pool, same stride): the
+ *     tensor-memory kernel -- tcgen05.mma, M=128 rows x N=64, accumulators in
+ *     tensor memory, up to 32 query heads per CTA; separate values: as 2.
+ *   1 CUDA cores, f32 arithmetic, 8 query heads per CTA.
+ *   2 warp-level tensor cores (mma.sync m16n8k16), 8 query heads per CTA.
+ * Every tensor-core path splits q and P into hi + lo 16-bit halves and
+ * accumulates in f32.  The 8-head kernels regroup the plan's query heads at
+ * launch; the plan's chunks are used as they are.
+ *   plan        from pa_v2_plan with head_dim = Dim = 512 (up to 32 query heads
+ *               per CTA, pa_v2_q_heads_per_cta); stack_members and
+ *               out_row_step 1; kernel 0, 1 or 2 (else PA_EINVAL).
+ * A one-request plan given num_indices == plan->num_indices reads no chunk
+ * arrays or indptr, as in pa_v2_decode_partial.
  *   q [batch, num_qo_heads, 512] f32 (16-byte aligned), q_extra [batch,
  *   num_qo_heads, 64] f32 (8-byte aligned).
  *   extra_dim   must be 64 (ExtraDim).
