@@ -73,7 +73,7 @@ typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 #define PA_DEVICE_BAD_SLOT      0x2  /* a page slot outside [0, num_indices) */
 #define PA_DEVICE_BAD_PAGE      0x4  /* a page id outside [0, num_pages) */
 #define PA_DEVICE_BAD_INDPTR    0x8  /* o_indptr decreasing or outside [0, num_partials] */
-#define PA_DEVICE_WAIT_TIMEOUT  0x10 /* a bounded wait for staged K/V gave up */
+#define PA_DEVICE_WAIT_TIMEOUT  0x10 /* a bounded wait (staged K/V, a tensor-memory kernel role) gave up */
 #define PA_DEVICE_BAD_BLOCK     0x20 /* a selected block id outside the scored range */
 
 /* Largest chunk count of any plan: the 65535 grid-z bound of the pages'
@@ -300,6 +300,16 @@ pa_status pa_v2_decode_partial_extra(const pa_v2_plan_t* plan, const float* q, c
                                      const int32_t* request_indices, const int32_t* kv_tile_indices,
                                      float sm_scale, float* v_out, float* lse2_out, int32_t* status,
                                      void* cuda_stream);
+
+/* Self-test of the tensor-memory kernel's bounded waits, for failure-detection
+ * tests (no tensor memory, no copies, one CTA of 2 warps): warp 0 waits on an
+ * mbarrier nothing arrives on for about limit_cycles SM clocks, gives up,
+ * records PA_DEVICE_WAIT_TIMEOUT in *status and raises the CTA's abort flag;
+ * warp 1 waits on another with the kernels' full limit (about 2^31 cycles) and
+ * must give up through that flag.  completed[2] (device int32) receives 1 for a
+ * warp whose wait completed (neither may).  status, completed: DEVICE pointers.
+ * PA_EINVAL for limit_cycles outside [1024, 2^31]. */
+pa_status pa_v2_selftest_wait(int32_t* status, int32_t* completed, int64_t limit_cycles, void* cuda_stream);
 
 /* Block-sparse selections (sparse-paged-decode.md, issue #904: the paragraphs
  * on selection_from_blocks and on the final block).  A model that scores

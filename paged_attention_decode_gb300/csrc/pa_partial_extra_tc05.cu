@@ -194,7 +194,7 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 // Bounded wait that also gives up once another role has given up (abort flag);
 // warp-uniform result.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
-                                           int32_t* status) {
+                                           int32_t* status, long long limit = kWaitLimitCycles) {
   bool ok = mbar_try_wait(bar, parity);
   if (!ok) {
     const long long t0 = clock64();
@@ -204,7 +204,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
         break;
       }
       if (*abort) break;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *abort = 1u;
         report(status, PA_DEVICE_WAIT_TIMEOUT);
         break;
@@ -613,6 +613,28 @@ __global__ void __launch_bounds__(kTThreads, 1)
   }
 }
 
+// Self-test of the waits above (no tensor memory, no copies): warp 0 waits on a
+// barrier nothing arrives on with a short limit and gives up; warp 1 waits on
+// another with the full limit and must give up through the abort flag warp 0
+// set.  completed[w] = 1 if warp w's wait returned true (it must not).
+__global__ void __launch_bounds__(64, 1) pa_selftest_wait_kernel(int32_t* status, int32_t* completed,
+                                                                  long long short_limit) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    abort_word = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  volatile uint32_t* abort_flag = &abort_word;
+  const bool ok = warp == 0 ? wait_phase(&bars[0], 0, abort_flag, status, short_limit)
+                            : wait_phase(&bars[1], 0, abort_flag, status, kWaitLimitCycles);
+  if ((threadIdx.x & 31) == 0) completed[warp] = ok ? 1 : 0;
+}
+
 using Tc05Kernel = void (*)(const PartialParams, const Tc05Fields);
 
 Tc05Kernel tc05_pick(int kv_dtype) {
@@ -647,3 +669,11 @@ int launch_partial_extra_tc05(const PartialParams& p, const void* q_extra, const
 }
 
 }  // namespace pa
+
+extern "C" pa_status pa_v2_selftest_wait(int32_t* status, int32_t* completed, int64_t limit_cycles,
+                                         void* cuda_stream) {
+  if (!status || !completed || limit_cycles < 1024 || limit_cycles > pa::kWaitLimitCycles) return PA_EINVAL;
+  pa::pa_selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(cuda_stream)>>>(status, completed,
+                                                                                    (long long)limit_cycles);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+}

@@ -33,7 +33,7 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
                "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
-               "pa_v2_decode_partial_extra",
+               "pa_v2_decode_partial_extra", "pa_v2_selftest_wait",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_decode_partial_extra.argtypes = [PP, P, P, P, i64, P, i64, P, i64, i32, i32, i64, P, i64, P, P, P,
                                                  P, P, f32, P, P, P, P]
         L.pa_v2_decode_partial_extra.restype = i32
+        L.pa_v2_selftest_wait.argtypes = [P, P, i64, P]
+        L.pa_v2_selftest_wait.restype = i32
         L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
         L.pa_selection_rows_per_request.restype = i64
         L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
@@ -584,3 +586,13 @@ def decode_extra(plan: Plan, q, q_extra, k_pool, v_pool, k_extra_pool, indices, 
                                         last_page_len, first_page_offset, sm_scale, wv, wl, status, stream, ri, ti)
     return pa_merge_states(wv, wl, oi, s.batch, out, lse2, status, stream)
 
+
+
+def pa_v2_selftest_wait(status, completed, limit_cycles: int, stream=None):
+    """Bounded-wait self-test (pa_v2_selftest_wait): status int32 [1] and completed int32 [2], device tensors."""
+    for name, t, n in (("status", status, 1), ("completed", completed, 2)):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of >= {n} elements")
+    rc = lib().pa_v2_selftest_wait(status.data_ptr(), completed.data_ptr(), int(limit_cycles), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_selftest_wait")

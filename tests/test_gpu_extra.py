@@ -126,3 +126,45 @@ def test_head_dim_512_plans_are_refused_by_the_single_stream_kernel():
         pa.pa_v2_decode_partial(plan, d.q, d.k_pool[..., :D].contiguous(), d.k_pool[..., :D].contiguous(), d.indices,
                                 d.indptr, d.last_page_len, d.first_page_offset, 0.1)
     assert e.value.status == pa.PA_EUNSUPPORTED
+
+
+def test_out_of_range_page_id_is_reported_by_the_second_k_stream_kernels():
+    for kernel in (0, 2):
+        x = _paged([300, 90], [0, 0], 1, 32, 1, torch.bfloat16, seed=95)
+        b = x.batch
+        dt = pa.KV_DTYPES[b.dtype]
+        plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 1, 32, 1, D, dt, 16, 0, b.seq_lens)
+        plan.struct.kernel = kernel
+        d = x.to("cuda")
+        db = d.batch
+        bad = db.indices.clone()
+        bad[5] = b.k_pool.shape[0]          # one past the pool
+        bad[310] = -3
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_v2_decode_partial_extra(plan, db.q, d.q_extra, db.k_pool, db.v_pool, d.k_extra_pool, bad, db.indptr,
+                                      db.last_page_len, db.first_page_offset, 0.05, status=status)
+        torch.cuda.synchronize()
+        word = int(status.item())
+        assert word & pa.DEVICE_BAD_PAGE and pa.pa_status_from_device(word) == pa.PA_EOOB, (kernel, word)
+    # the context is still usable and a clean call is exact
+    _check(_paged([300, 90], [0, 0], 1, 32, 1, torch.bfloat16, seed=95), override=64)
+
+
+def test_bounded_wait_gives_up_and_the_other_role_follows():
+    """The tensor-memory kernel's wait: one warp's wait times out after ~2^20 cycles and raises the abort
+    flag; the other warp, waiting with the full ~2^31-cycle limit, leaves through the flag long before it."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    completed = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pa.pa_v2_selftest_wait(status, completed, 1 << 20)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == pa.DEVICE_WAIT_TIMEOUT
+    assert pa.pa_status_from_device(int(status.item())) == pa.PA_ECUDA
+    assert completed.tolist() == [0, 0]
+    assert elapsed < 0.5, elapsed
+    with pytest.raises(pa.PaError):
+        pa.pa_v2_selftest_wait(status, completed, 10)
+    _check(_paged([200], [0], 1, 32, 1, torch.bfloat16, seed=96), override=128)
