@@ -388,6 +388,26 @@ pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* host_in, void*
                             const int32_t* o_indptr, float sm_scale, float* workspace_v, float* workspace_lse,
                             void* cuda_stream);
 
+/* pa_v2_decode_host as one CUDA graph, for callers that repeat the step with
+ * the same buffers.  create() captures the step (input copy, partial kernel,
+ * merge when plan->needs_merge, output copy) into a graph and instantiates it;
+ * the plan (copied), host_in, host_out, dev_io, the pools, the chunk arrays,
+ * the workspaces and sm_scale are bound then, with the arguments and checks of
+ * pa_v2_decode_host.  run() checks the plan against the page table now in
+ * host_in (PA_EGEOMETRY, nothing launched), launches the graph on cuda_stream,
+ * waits for it and returns pa_status_from_device of the status word, like
+ * pa_v2_decode_host; host_in's 16-byte status slot must stay zero.  The bound
+ * buffers must outlive the graph; destroy() releases it (null is a no-op).
+ * One graph must not run on two streams at once. */
+typedef struct pa_v2_host_graph pa_v2_host_graph_t;
+pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                                  const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                  const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                  const int32_t* o_indptr, float sm_scale, float* workspace_v, float* workspace_lse,
+                                  pa_v2_host_graph_t** graph);
+pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* graph, void* cuda_stream);
+void pa_v2_host_graph_destroy(pa_v2_host_graph_t* graph);
+
 /* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
  * by every GPU that loads this library until the process exits. */
 #define PA_V2_NOALLOC_SCRATCH_BYTES (8u << 20)

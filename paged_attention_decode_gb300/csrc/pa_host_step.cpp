@@ -35,11 +35,16 @@ extern "C" pa_status pa_v2_host_io_layout(const pa_v2_plan_t* plan, int64_t* in_
   return PA_OK;
 }
 
-extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
-                                       const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
-                                       const int32_t* request_indices, const int32_t* kv_tile_indices,
-                                       const int32_t* o_indptr, float sm_scale, float* workspace_v,
-                                       float* workspace_lse, void* cuda_stream) {
+namespace {
+
+// Queue one host step on `stream` without waiting: the input copy, the partial
+// kernel (and the merge when the plan needs one), the output copy.  Checks the
+// arguments and the plan against the step's page table first.
+pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                            const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                            const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                            float sm_scale, float* workspace_v, float* workspace_lse, cudaStream_t stream,
+                            bool check_geometry) {
   int64_t in_bytes = 0, out_bytes = 0, io_bytes = 0;
   if (pa_v2_host_io_layout(plan, &in_bytes, &out_bytes, &io_bytes) != PA_OK) return PA_EINVAL;
   if (!host_in || !host_out || !dev_io || (reinterpret_cast<uintptr_t>(dev_io) & 15u)) return PA_EINVAL;
@@ -53,9 +58,8 @@ extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* hos
   const int32_t* h_indptr = h_words + q_words + plan->num_indices;
   const int32_t* h_lpl = h_indptr + B + 1;
   const int32_t* h_fpo = h_lpl + B;
-  if (!pa_v2_plan_matches(plan, h_indptr, h_lpl, h_fpo, B)) return PA_EGEOMETRY;
+  if (check_geometry && !pa_v2_plan_matches(plan, h_indptr, h_lpl, h_fpo, B)) return PA_EGEOMETRY;
 
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   unsigned char* io = static_cast<unsigned char*>(dev_io);
   if (cudaMemcpyAsync(io, host_in, (size_t)in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return PA_ECUDA;
 
@@ -68,27 +72,122 @@ extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* hos
   int32_t* status = reinterpret_cast<int32_t*>(out_region);
   float* out = reinterpret_cast<float*>(out_region + 16);
   float* lse = out + q_words;
+  void* cs = static_cast<void*>(stream);
 
   pa_status rc;
   if (plan->needs_merge) {
     rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
-                              fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse, status,
-                              cuda_stream);
+                              fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse, status, cs);
     if (rc == PA_OK)
       rc = pa_merge_states(workspace_v, workspace_lse, o_indptr, B, plan->num_chunks, plan->num_qo_heads,
-                           plan->head_dim, out, lse, status, cuda_stream);
+                           plan->head_dim, out, lse, status, cs);
   } else {
     rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
-                              fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cuda_stream);
+                              fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cs);
   }
+  if (rc != PA_OK) return rc;
+  if (cudaMemcpyAsync(host_out, out_region, (size_t)out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PA_ECUDA;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                                       const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                       const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                       const int32_t* o_indptr, float sm_scale, float* workspace_v,
+                                       float* workspace_lse, void* cuda_stream) {
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
+                                         request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v,
+                                         workspace_lse, stream, true);
   if (rc != PA_OK) {
     cudaStreamSynchronize(stream);  // the input copy may still be reading host_in
     return rc;
   }
-  if (cudaMemcpyAsync(host_out, out_region, (size_t)out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess)
-    return PA_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
   int32_t word = 0;
   std::memcpy(&word, host_out, sizeof(word));
   return pa_status_from_device(word);
+}
+
+// ---- the same step as one CUDA graph ---------------------------------------
+//
+// Per step the direct call above issues two copies and two launches through
+// the runtime; the graph replays them with one launch.  Everything except the
+// contents of host_in is bound when the graph is made: the plan (a copy), the
+// buffers, the pools, the chunk arrays, the scale.  Capture runs on a private
+// stream; the programmatic launches of the partial and merge kernels become
+// programmatic edges of the graph.
+
+struct pa_v2_host_graph {
+  pa_v2_plan_t plan;
+  const void* host_in;
+  void* host_out;
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+extern "C" pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
+                                             void* dev_io, const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                                             int64_t num_pages, const int32_t* request_indices,
+                                             const int32_t* kv_tile_indices, const int32_t* o_indptr, float sm_scale,
+                                             float* workspace_v, float* workspace_lse, pa_v2_host_graph_t** out) {
+  if (!plan || !out) return PA_EINVAL;
+  *out = nullptr;
+  cudaStream_t cap = nullptr;
+  if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return PA_ECUDA;
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(cap);
+    return PA_ECUDA;
+  }
+  // the geometry is checked on every run, against that step's page table
+  pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
+                                   request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse,
+                                   cap, false);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
+  cudaStreamDestroy(cap);
+  if (rc == PA_OK && (ec != cudaSuccess || !graph)) rc = PA_ECUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (rc == PA_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = PA_ECUDA;
+  if (rc != PA_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return rc;
+  }
+  pa_v2_host_graph_t* g = new pa_v2_host_graph_t;
+  g->plan = *plan;
+  g->host_in = host_in;
+  g->host_out = host_out;
+  g->graph = graph;
+  g->exec = exec;
+  *out = g;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* g, void* cuda_stream) {
+  if (!g) return PA_EINVAL;
+  const pa_v2_plan_t* plan = &g->plan;
+  const int32_t B = plan->batch;
+  const int32_t* h_words = static_cast<const int32_t*>(g->host_in);
+  const int32_t* h_indptr = h_words + (int64_t)B * plan->num_qo_heads * plan->head_dim + plan->num_indices;
+  if (!pa_v2_plan_matches(plan, h_indptr, h_indptr + B + 1, h_indptr + 2 * B + 1, B)) return PA_EGEOMETRY;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaGraphLaunch(g->exec, stream) != cudaSuccess) {
+    cudaStreamSynchronize(stream);
+    return PA_ECUDA;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
+  int32_t word = 0;
+  std::memcpy(&word, g->host_out, sizeof(word));
+  return pa_status_from_device(word);
+}
+
+extern "C" void pa_v2_host_graph_destroy(pa_v2_host_graph_t* g) {
+  if (!g) return;
+  cudaGraphExecDestroy(g->exec);
+  cudaGraphDestroy(g->graph);
+  delete g;
 }

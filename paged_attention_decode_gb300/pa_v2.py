@@ -33,7 +33,8 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_v2_decode_partial", "pa_v2_decode", "pa_v2_decode_noalloc", "pa_merge_states",
                "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
-               "pa_v2_decode_partial_extra", "pa_v2_selftest_wait",
+               "pa_v2_decode_partial_extra", "pa_v2_selftest_wait", "pa_v2_host_graph_create",
+               "pa_v2_host_graph_run", "pa_v2_host_graph_destroy",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -97,6 +98,12 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_decode_partial_extra.restype = i32
         L.pa_v2_selftest_wait.argtypes = [P, P, i64, P]
         L.pa_v2_selftest_wait.restype = i32
+        L.pa_v2_host_graph_create.argtypes = [PP, P, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
+        L.pa_v2_host_graph_create.restype = i32
+        L.pa_v2_host_graph_run.argtypes = [P, P]
+        L.pa_v2_host_graph_run.restype = i32
+        L.pa_v2_host_graph_destroy.argtypes = [P]
+        L.pa_v2_host_graph_destroy.restype = None
         L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
         L.pa_selection_rows_per_request.restype = i64
         L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
@@ -486,9 +493,11 @@ class HostStep:
 
     pack(q, indices, indptr, last_page_len, first_page_offset) writes a step's host inputs into the pinned
     input buffer (or pass prepacked=True to run() after filling `host_in` yourself); run() makes the one
-    C call and returns (out [B, Hq, D], lse2 [B, Hq]) as views of the pinned output buffer."""
+    C call and returns (out [B, Hq, D], lse2 [B, Hq]) as views of the pinned output buffer.
+    graph_scale: also capture the step as a CUDA graph (pa_v2_host_graph_create) bound to this scale;
+    run() with that scale then replays it (pa_v2_host_graph_run)."""
 
-    def __init__(self, plan: Plan, k_pool, v_pool, stream=None):
+    def __init__(self, plan: Plan, k_pool, v_pool, stream=None, graph_scale=None):
         s = plan.struct
         self.plan = plan
         dev = k_pool.device
@@ -511,6 +520,21 @@ class HostStep:
                       _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"), KV_DTYPES[k_pool.dtype],
                       k_pool.shape[0], ri.data_ptr(), ti.data_ptr(), oi.data_ptr())
         self._tail = (self.ws[0].data_ptr(), self.ws[1].data_ptr(), _stream(stream))
+        self._graph = None
+        self._graph_scale = None
+        if graph_scale is not None:
+            g = ctypes.c_void_p()
+            rc = lib().pa_v2_host_graph_create(*self._args, float(graph_scale), self.ws[0].data_ptr(),
+                                               self.ws[1].data_ptr(), ctypes.byref(g))
+            if rc != PA_OK:
+                raise PaError(rc, "pa_v2_host_graph_create")
+            self._graph, self._graph_scale = g, float(graph_scale)
+            self._lib = lib()
+
+    def __del__(self):
+        if getattr(self, "_graph", None) is not None:
+            self._lib.pa_v2_host_graph_destroy(self._graph)
+            self._graph = None
 
     def pack(self, q, indices, indptr, last_page_len, first_page_offset):
         """Copy one step's inputs (host tensors) into the pinned input buffer."""
@@ -523,6 +547,11 @@ class HostStep:
         w[o:] = 0
 
     def run(self, sm_scale: float):
+        if self._graph is not None and float(sm_scale) == self._graph_scale:
+            rc = self._lib.pa_v2_host_graph_run(self._graph, self._tail[2])
+            if rc != PA_OK:
+                raise PaError(rc, "pa_v2_host_graph_run")
+            return self.out, self.lse
         rc = self._fn(*self._args, float(sm_scale), *self._tail)
         if rc != PA_OK:
             raise PaError(rc, "pa_v2_decode_host")

@@ -372,7 +372,8 @@ def test_autotune_times_candidates_and_tuned_plan_is_exact(fused):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["tiny_csr", "sliding_window_batch", "nomerge"])
-def test_host_step_matches_the_device_path(name):
+@pytest.mark.parametrize("graph", [False, True])
+def test_host_step_matches_the_device_path(name, graph):
     if name == "nomerge":
         b = W.make_batch("nomerge", [40, 17, 0], [0, 3, 0], 16, 8, 2, 128, torch.float16, seed=23)
         plan = make_plan(b, target=1)
@@ -381,7 +382,7 @@ def test_host_step_matches_the_device_path(name):
         b = W.WORKLOADS[name]()
         plan = make_plan(b)
     d = b.to("cuda")
-    step = pa.HostStep(plan, d.k_pool, d.v_pool)
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None)
     step.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
     for _ in range(2):                                  # the status slot is re-zeroed by every copy
         o, l = step.run(b.scale)
@@ -393,11 +394,12 @@ def test_host_step_matches_the_device_path(name):
     assert torch.equal(o2.cpu(), o) and torch.equal(l2.cpu(), l)
 
 
-def test_host_step_refuses_a_stale_plan_and_reports_bad_pages():
+@pytest.mark.parametrize("graph", [False, True])
+def test_host_step_refuses_a_stale_plan_and_reports_bad_pages(graph):
     b = W.make_batch("hs", [100, 60], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
     plan = make_plan(b, target=16)
     d = b.to("cuda")
-    step = pa.HostStep(plan, d.k_pool, d.v_pool)
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None)
     grown = W.make_batch("hs", [100, 90], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
     step.pack(grown.q, grown.indices[:b.indices.numel()], grown.indptr, grown.last_page_len,
               grown.first_page_offset)
@@ -415,3 +417,20 @@ def test_host_step_refuses_a_stale_plan_and_reports_bad_pages():
     ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                     b.first_page_offset, b.scale)
     assert_close(o.clone(), l.clone(), ref_o, ref_l, "host step after errors")
+
+
+def test_host_graph_replays_new_inputs_and_other_scales_take_the_direct_path():
+    """The graph binds buffers and scale; each run reads the step's current host inputs."""
+    sets = [W.make_batch("hg", [300, 200], [0, 5], 16, 8, 2, 128, torch.float16, seed=s) for s in (31, 32)]
+    b0 = sets[0]
+    plan = make_plan(b0, target=32)
+    d = b0.to("cuda")
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b0.scale)
+    for b in sets:  # same geometry and pool; new q and a new page permutation of the same pool
+        q = b.q
+        step.pack(q, b0.indices.flip(0).contiguous(), b0.indptr, b0.last_page_len, b0.first_page_offset)
+        for scale in (b0.scale, 0.5 * b0.scale):
+            o, l = step.run(scale)
+            ref_o, ref_l = oracle.attention(q, b0.k_pool, b0.v_pool, b0.indices.flip(0).contiguous(), b0.indptr,
+                                            b0.last_page_len, b0.first_page_offset, scale)
+            assert_close(o.clone(), l.clone(), ref_o, ref_l, f"host graph scale {scale}")
