@@ -594,6 +594,13 @@ def run_workload(args):
 
     d = b.to(dev)
     plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, b.ppc_override)
+    chunking = "fixed by the workload" if b.ppc_override else "pa_v2_plan's search"
+    wave = pa.pa_v2_default_target_ctas(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, dt)
+    if not b.ppc_override and not cascade and plan.total_ctas > wave:
+        # the search's chunk size spills past one wave: take the smallest size that fits it
+        fit = pa.pa_v2_wave_fit_pages_per_chunk(b.indptr, plan.q_groups * plan.num_kv_heads, wave)
+        plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, fit)
+        chunking = "pa_v2_wave_fit_pages_per_chunk (the search's size spilled past one wave)"
     tuned = None
     if args.tune and not cascade:
         from paged_attention_decode_gb300 import autotune
@@ -601,6 +608,7 @@ def run_workload(args):
         if tuned.pages_per_chunk != plan.pages_per_chunk:
             plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens,
                              tuned.pages_per_chunk)
+        chunking = "autotuned"
     out = torch.empty(b.batch, b.num_qo_heads, b.head_dim, device=dev)
     lse = torch.empty(b.batch, b.num_qo_heads, device=dev)
 
@@ -713,6 +721,7 @@ def run_workload(args):
                        "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
                        "kv_dtype": str(b.dtype).replace("torch.", ""), "seq_lens_total": sum(b.seq_lens),
                        "num_chunks": plan.num_chunks, "pages_per_chunk": plan.pages_per_chunk,
+                       "chunking": chunking,
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
     if tuned is not None:

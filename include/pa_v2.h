@@ -161,6 +161,17 @@ pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len,
 /* 1 if `plan` is still valid for this geometry (same batch and per-request
  * page counts, and a geometry that passes the checks of pa_v2_plan); else 0.
  * Host pointers. */
+/* The smallest pages_per_chunk whose CTA count -- sum over requests of
+ * max(1, ceil(pages_r / ppc)) * ctas_per_chunk, pages_r = indptr[r+1] -
+ * indptr[r] -- is at most `wave`; pass it to pa_v2_plan as
+ * pages_per_chunk_override.  pa_v2_plan's own search takes the largest size
+ * that still reaches its target, so its CTA count can pass one wave (one CTA
+ * per SM) by up to a chunk per request.  Returns the one-chunk-per-request
+ * size when even that does not fit, 0 for bad arguments.  Host pointers;
+ * ctas_per_chunk = num_kv_heads * q_groups of the plan. */
+int32_t pa_v2_wave_fit_pages_per_chunk(const int32_t* indptr, int32_t batch, int32_t ctas_per_chunk,
+                                       int32_t wave);
+
 int32_t pa_v2_plan_matches(const pa_v2_plan_t* plan, const int32_t* indptr,
                            const int32_t* last_page_len, const int32_t* first_page_offset,
                            int32_t batch);

@@ -185,6 +185,40 @@ const char* pa_status_string(int32_t s) {
   }
 }
 
+// The smallest chunk size whose CTAs fit one wave.  The plan's binary search
+// takes the largest chunk size that still reaches the target, so its CTA count
+// may pass the target by up to one chunk per request; with one CTA per SM the
+// extra CTAs then run as a second, almost empty wave.  CTA count of a size s:
+// sum over requests of max(1, ceil(pages_r / s)) * ctas_per_chunk.
+int32_t pa_v2_wave_fit_pages_per_chunk(const int32_t* indptr, int32_t batch, int32_t ctas_per_chunk,
+                                       int32_t wave) {
+  if (!indptr || batch < 1 || ctas_per_chunk < 1 || wave < 1 || indptr[0] != 0) return 0;
+  int32_t longest = 1;
+  for (int32_t r = 0; r < batch; ++r) {
+    const int32_t n = indptr[r + 1] - indptr[r];
+    if (n < 0) return 0;
+    if (n > longest) longest = n;
+  }
+  auto ctas = [&](int32_t size) {
+    int64_t chunks = 0;
+    for (int32_t r = 0; r < batch; ++r) {
+      const int64_t n = indptr[r + 1] - indptr[r];
+      chunks += n <= size ? 1 : (n + size - 1) / size;
+    }
+    return chunks * ctas_per_chunk;
+  };
+  if (ctas(longest) > wave) return longest;  // one chunk per request does not fit either
+  int32_t lo = 1, hi = longest;
+  while (lo < hi) {
+    const int32_t mid = lo + (hi - lo) / 2;
+    if (ctas(mid) <= wave)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
 const char* pa_version(void) { return "pa_v2 0.1 (sm_103a)"; }
 
 }  // extern "C"

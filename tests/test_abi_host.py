@@ -226,3 +226,41 @@ def test_host_io_layout_sizes():
     assert i == -(-words * 4 // 16) * 16 + 16 and i % 16 == 0
     assert o == 16 + b.q.numel() * 4 + b.batch * b.num_qo_heads * 4
     assert io == i - 16 + o
+
+
+def _ctas(pages, size, per):
+    return sum(max(1, -(-p // size)) for p in pages) * per
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_wave_fit_is_the_smallest_size_that_fits(seed):
+    """Brute force over every chunk size: the result fits the wave and the size one below does not (or the
+    result is the one-chunk-per-request size when nothing fits); it agrees with the Python helper."""
+    import random
+    from paged_attention_decode_gb300 import cascade as C
+    rng = random.Random(seed)
+    pages = [rng.choice([0, 1, 7, 64, 113, 2048, rng.randint(0, 3000)]) for _ in range(rng.randint(1, 9))]
+    indptr = [0]
+    for p in pages:
+        indptr.append(indptr[-1] + p)
+    for per, wave in ((1, 152), (8, 152), (4, 144), (16, 20), (3, 7)):
+        got = pa.pa_v2_wave_fit_pages_per_chunk(indptr, per, wave)
+        longest = max([1] + pages)
+        if _ctas(pages, longest, per) > wave:
+            assert got == longest
+        else:
+            assert _ctas(pages, got, per) <= wave
+            assert got == 1 or _ctas(pages, got - 1, per) > wave
+            assert got == min(s for s in range(1, longest + 1) if _ctas(pages, s, per) <= wave)
+        assert got == C.fit_pages_per_chunk(pages, per, wave)
+
+
+def test_wave_fit_on_the_sparse_shape_and_bad_arguments():
+    # 16 requests of 2048 single-row pages, 1 KV head: the plan's search takes 227 pages (160 CTAs);
+    # one wave of 152 holds 9 chunks per request (144 CTAs) at 228 pages
+    indptr = [2048 * r for r in range(17)]
+    assert pa.pa_v2_wave_fit_pages_per_chunk(indptr, 1, 152) == 228
+    with pytest.raises(pa.PaError):
+        pa.pa_v2_wave_fit_pages_per_chunk([0, 5], 0, 152)
+    with pytest.raises(pa.PaError):
+        pa.pa_v2_wave_fit_pages_per_chunk([1, 5], 1, 152)
