@@ -17,6 +17,8 @@
 // 128 / 32 CTAs instead of 128 / 8.
 //
 // 288 threads in three roles:
+//  - q: one 2 KB bulk copy per head (the copy engine) into the latent blocks the
+//    first tile fills last, converted to hi + lo halves by the other 160 threads.
 //  - warps 0-3, loaders: gather the chunk's rows 128 at a time with cp.async
 //    into a tile of nine 128-byte-swizzled blocks [128 rows x 64 dims] (blocks
 //    0-7 the latent dims, block 8 the extra dims), 8 lanes per row and one
@@ -83,7 +85,7 @@ constexpr int kTOffQ = kTOffK + kTBlocks * kTBlockBytes;   // 147456
 constexpr int kTOffRed = kTOffQ + kTBlocks * kTQBlockBytes;  // 221184: [2][4][32] f32
 constexpr int kTOffBar = kTOffRed + 2 * 4 * kTHeads * 4;   // 222208
 static_assert(2 * kTPBlockBytes == kTBlockBytes, "P^T fills the extra block");
-constexpr int kTNumBars = 17;
+constexpr int kTNumBars = 19;
 constexpr int kTOffMisc = kTOffBar + kTNumBars * 8;        // tensor-memory address, abort flag
 constexpr int kTSmem = kTOffMisc + 16;
 constexpr int kTSmemAlloc = kTSmem + 1024;                 // room to align the base
@@ -96,6 +98,10 @@ constexpr int kBarP = 10;        // P^T written, S^T read, O^T rescaled (128 sof
 constexpr int kBarPv = 11;       // 4: O^T m-tile j complete (commit): blocks 2j, 2j+1 (and, j = 3, 8) free
 constexpr int kBarRed = 15;      // the softmax warps' exchange (128 arrivals)
 constexpr int kBarDrain = 16;    // all MMAs complete (commit), before tensor memory is released
+constexpr int kBarQ = 17;        // the f32 q rows have landed in the staging area (bulk copies)
+constexpr int kBarQc = 18;       // [Q_hi ; Q_lo]^T is written (the 160 non-loader threads)
+constexpr int kTQThreads = kTThreads - kTLoadWarps * 32;
+constexpr int kTOffQStage = kTOffK + 4 * kTBlockBytes;  // f32 q rows, 32 x 2 KB, in latent blocks 4-7
 
 // tensor-memory columns
 constexpr uint32_t kTmemCols = 512;
@@ -166,6 +172,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
                "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
                PA_W32(r)
+               : "memory");
+}
+
+// One contiguous global -> shared copy on the copy engine, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
 }
 
@@ -264,6 +277,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
     for (int j = 0; j < 4; ++j) mbar_init(&bars[kBarPv + j], 1);
     mbar_init(&bars[kBarRed], 128);
     mbar_init(&bars[kBarDrain], 1);
+    mbar_init(&bars[kBarQ], 1);
+    mbar_init(&bars[kBarQc], kTQThreads);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -311,67 +326,64 @@ __global__ void __launch_bounds__(kTThreads, 1)
   int64_t prow[8], pnext[8];
   if (warp < kTLoadWarps && n_tiles > 0) lookup(0, pnext);
 
-  // ---- [Q_hi ; Q_lo]^T by all threads: block b holds dims 64b .. 64b+63 of 32 hi rows then 32 lo
-  // rows.  Items are 4 q values (16-byte loads) or 2 q_extra values (8-byte loads); a thread issues
-  // its loads 9 at a time before its shared-memory stores, so they overlap.
-  {
+  // ---- [Q_hi ; Q_lo]^T.  The f32 q rows go to the copy engine (one 2 KB bulk copy per head into
+  // latent blocks 4-7, which the first tile does not load until the tile is converted), so they do
+  // not queue behind the loaders' row copies; q_extra (8 KB, 8-byte aligned) is read directly.  The
+  // 160 non-loader threads convert: block b holds dims 64b .. 64b+63 of 32 hi rows then 32 lo rows.
+  bool q_ok = true;
+  if (warp >= kTLoadWarps) {
+    if (warp == kTMmaWarp) {
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarQ], (uint32_t)(nheads * kTDim * 4));
+      __syncwarp();
+      if (lane < nheads)
+        bulk_g2s(sbase + kTOffQStage + lane * (kTDim * 4),
+                 p.q + ((size_t)r * p.num_qo_heads + h_first + lane) * kTDim, kTDim * 4, &bars[kBarQ]);
+    }
+    const int tq = threadIdx.x - kTLoadWarps * 32;
     unsigned char* qt = smem + kTOffQ;
-    constexpr int kQItems = kTHeads * (kTDim / 4);               // 4096 float4 of q
-    constexpr int kItems = kQItems + kTHeads * (kTExtra / 2);   // + 1024 float2 of q_extra
-    constexpr int kBatch = 9;
-#pragma unroll 1
-    for (int base = 0; base < kItems; base += kBatch * kTThreads) {
-      float4 qv[kBatch];
+    auto put = [&](int h, int d, float a, float b) {  // dims d, d + 1 of head h (d even)
+      const float v0 = a * p.scale_log2, v1 = b * p.scale_log2;
+      const float h0 = TC<T>::round(v0), h1 = TC<T>::round(v1);
+      const int dd = d & 63;
+      unsigned char* blk = qt + (d >> 6) * kTQBlockBytes;
+      const uint32_t off = sw128(h, dd >> 3) + (dd & 7) * 2;  // rows h and h + 32 share the swizzle phase
+      *reinterpret_cast<uint32_t*>(blk + off) = (uint32_t)TC<T>::bits(h0) | ((uint32_t)TC<T>::bits(h1) << 16);
+      *reinterpret_cast<uint32_t*>(blk + kTHeads * 128 + off) =
+          (uint32_t)TC<T>::bits(v0 - h0) | ((uint32_t)TC<T>::bits(v1 - h1) << 16);
+    };
+    // q_extra: 32 heads x 32 float2, loads first
+    constexpr int kE = kTHeads * (kTExtra / 2);
+    constexpr int kEPer = (kE + kTQThreads - 1) / kTQThreads;
+    float2 ev[kEPer];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int it = base + (int)threadIdx.x + k * kTThreads;
-        qv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (it < kQItems) {
-          const int h = it >> 7;
-          if (h < nheads)
-            qv[k] = __ldg(reinterpret_cast<const float4*>(p.q + ((size_t)r * p.num_qo_heads + h_first + h) * kTDim +
-                                                          (it & 127) * 4));
-        } else if (it < kItems) {
-          const int h = (it - kQItems) >> 5;
-          if (h < nheads) {
-            const float2 e2 = __ldg(reinterpret_cast<const float2*>(
-                x.q_extra + ((size_t)r * p.num_qo_heads + h_first + h) * kTExtra + ((it - kQItems) & 31) * 2));
-            qv[k].x = e2.x;
-            qv[k].y = e2.y;
-          }
-        }
+    for (int k = 0; k < kEPer; ++k) {
+      const int it = tq + k * kTQThreads;
+      const int h = it >> 5;
+      ev[k] = make_float2(0.f, 0.f);
+      if (it < kE && h < nheads)
+        ev[k] = __ldg(reinterpret_cast<const float2*>(x.q_extra + ((size_t)r * p.num_qo_heads + h_first + h) * kTExtra +
+                                                      (it & 31) * 2));
+    }
+    q_ok = wait_phase(&bars[kBarQ], 0, abort_flag, p.status);
+    if (q_ok) {
+      const float* stage = reinterpret_cast<const float*>(smem + kTOffQStage);
+      constexpr int kQ4 = kTHeads * (kTDim / 4);  // float4 items
+      for (int it = tq; it < kQ4; it += kTQThreads) {
+        const int h = it >> 7, d = (it & 127) * 4;
+        const float4 v = h < nheads ? *reinterpret_cast<const float4*>(stage + h * kTDim + d)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        put(h, d, v.x, v.y);
+        put(h, d + 2, v.z, v.w);
       }
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int it = base + (int)threadIdx.x + k * kTThreads;
-        if (it < kItems) {
-          const bool isq = it < kQItems;
-          const int h = isq ? it >> 7 : (it - kQItems) >> 5;
-          const int d = isq ? (it & 127) * 4 : kTDim + ((it - kQItems) & 31) * 2;
-          const float v0 = qv[k].x * p.scale_log2, v1 = qv[k].y * p.scale_log2;
-          const float v2 = qv[k].z * p.scale_log2, v3 = qv[k].w * p.scale_log2;
-          const float h0 = TC<T>::round(v0), h1 = TC<T>::round(v1), h2 = TC<T>::round(v2), h3 = TC<T>::round(v3);
-          const int dd = d & 63;
-          unsigned char* blk = qt + (d >> 6) * kTQBlockBytes;
-          const uint32_t off = sw128(h, dd >> 3) + (dd & 7) * 2;  // rows h and h + 32 share the swizzle phase
-          const uint32_t hi01 = (uint32_t)TC<T>::bits(h0) | ((uint32_t)TC<T>::bits(h1) << 16);
-          const uint32_t lo01 = (uint32_t)TC<T>::bits(v0 - h0) | ((uint32_t)TC<T>::bits(v1 - h1) << 16);
-          if (isq) {
-            const uint32_t hi23 = (uint32_t)TC<T>::bits(h2) | ((uint32_t)TC<T>::bits(h3) << 16);
-            const uint32_t lo23 = (uint32_t)TC<T>::bits(v2 - h2) | ((uint32_t)TC<T>::bits(v3 - h3) << 16);
-            *reinterpret_cast<uint2*>(blk + off) = make_uint2(hi01, hi23);
-            *reinterpret_cast<uint2*>(blk + kTHeads * 128 + off) = make_uint2(lo01, lo23);
-          } else {
-            *reinterpret_cast<uint32_t*>(blk + off) = hi01;
-            *reinterpret_cast<uint32_t*>(blk + kTHeads * 128 + off) = lo01;
-          }
-        }
+      for (int k = 0; k < kEPer; ++k) {
+        const int it = tq + k * kTQThreads;
+        if (it < kE) put(it >> 5, kTDim + (it & 31) * 2, ev[k].x, ev[k].y);
       }
     }
+    fence_proxy_async_smem();  // the q tile is read by the tensor cores
+    mbar_arrive(&bars[kBarQc]);
   }
-  fence_proxy_async_smem();  // the q tile is read by the tensor cores
-  __syncwarp();
-  __syncthreads();
 
   if (warp < kTLoadWarps) {
     // ------------------------------------------------------------------ loaders
@@ -386,6 +398,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
       for (int b = 0; b < kTBlocks; ++b) {
         if (i > 0 && (b & 1) == 0 && b < 8 &&
             !wait_phase(&bars[kBarPv + (b >> 1)], (uint32_t)((i - 1) & 1), abort_flag, p.status)) {
+          alive = false;
+          break;
+        }
+        // blocks 4-7 of the first tile held the f32 q rows until they were converted
+        if (i == 0 && b == 4 && !wait_phase(&bars[kBarQc], 0, abort_flag, p.status)) {
           alive = false;
           break;
         }
@@ -423,7 +440,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     constexpr uint32_t id_qk = instr_desc(fmt, 128, 64, false);
     constexpr uint32_t id_pv = instr_desc(fmt, 128, 64, true);
     const uint32_t k_addr = sbase + kTOffK, q_addr = sbase + kTOffQ, p_addr = sbase + kTOffP;
-    bool alive = true;
+    bool alive = q_ok && (n_tiles == 0 || wait_phase(&bars[kBarQc], 0, abort_flag, p.status));
     bool issued = false;
     for (int i = 0; i < n_tiles && alive; ++i) {
       const uint32_t par = (uint32_t)(i & 1);
@@ -482,7 +499,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
     for (int h = 0; h < kTHeads; ++h) l_part[h] = 0.f;
     float m_lane = -INFINITY;  // running maximum of head `lane`
-    bool alive = true;
+    bool alive = q_ok;
     unsigned char* pt = smem + kTOffP + (row >> 6) * kTPBlockBytes;
     for (int i = 0; i < n_tiles; ++i) {
       const uint32_t par = (uint32_t)(i & 1);
