@@ -15,9 +15,12 @@
 // entry (fpo + i) % ps; one CTA per (chunk, kv head, q-head group).
 //
 // Shapes served: Dim 512, ExtraDim 64 (DeepSeek's kv_lora_rank and
-// qk_rope_head_dim), up to 8 query heads per CTA, f16 / bf16 pools.  The
-// tensor-core variant (pa_partial_extra_tc.cu) is the default; this one runs
-// when plan.kernel == 1.
+// qk_rope_head_dim), 8 query heads per CTA, f16 / bf16 pools.  This file also
+// holds the entry point, which picks the kernel by plan.kernel: 0 the
+// tensor-memory kernel (pa_partial_extra_tc05.cu) when the values are the key
+// rows, else the warp-level tensor-core kernel (pa_partial_extra_tc.cu, also
+// plan.kernel 2); 1 this CUDA-core kernel.  The plans group up to 32 query
+// heads per CTA; the 8-head kernels regroup them at launch.
 //
 // Layout: 4 warps, each owning 2 of the CTA's query heads; all four read the
 // same K / V rows (the later ones from L1).  Lane l owns latent dims
