@@ -876,8 +876,14 @@ def run_crossover(args):
                              seed=1100 + B * 7 + ctx // 1024)
             d = b.to(dev)
             dt = pa.KV_DTYPES[b.dtype]
-            plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, ps, Hq, Hkv, D, dt,
-                                 pa.pa_v2_default_target_ctas(Hq, Hkv, D, ps, dt), 0, b.seq_lens)
+            wave = pa.pa_v2_default_target_ctas(Hq, Hkv, D, ps, dt)
+            plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, ps, Hq, Hkv, D, dt, wave, 0,
+                                 b.seq_lens)
+            search_ppc = plan.pages_per_chunk
+            if plan.total_ctas > wave:  # the search's size spills past one wave: the size that fits it
+                fit = pa.pa_v2_wave_fit_pages_per_chunk(b.indptr, plan.q_groups * plan.num_kv_heads, wave)
+                plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, ps, Hq, Hkv, D, dt, wave, fit,
+                                     b.seq_lens)
             out = torch.empty(B, Hq, D, device=dev)
             lse = torch.empty(B, Hq, device=dev)
             ws = (torch.empty(max(1, plan.num_chunks), Hq, D, device=dev),
@@ -900,6 +906,7 @@ def run_crossover(args):
             def contiguous():
                 return F.scaled_dot_product_attention(q16, kc, vc, scale=b.scale, enable_gqa=True)
 
+            stream.wait_stream(torch.cuda.current_stream())  # q16, kc, vc were built on the default stream
             with torch.cuda.stream(stream):
                 v2()
                 ref = contiguous()
@@ -908,6 +915,7 @@ def run_crossover(args):
             if not err <= 2e-2:
                 raise SystemExit(f"bench: crossover B={B} ctx={ctx}: v2 and SDPA disagree ({err:.3e})")
             cell = {"batch": B, "context": ctx, "pages_per_chunk": plan.pages_per_chunk,
+                    "search_pages_per_chunk": search_ppc, "ctas": plan.total_ctas,
                     "chunks": plan.num_chunks, "merge": bool(plan.needs_merge)}
             for name, fn in (("v2", v2), ("gather_sdpa", gather_sdpa), ("contiguous", contiguous)):
                 med, p10, p90 = _time_cold(fn, stream, flush, args.warmup, args.steps, args.graph)
