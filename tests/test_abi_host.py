@@ -264,3 +264,15 @@ def test_wave_fit_on_the_sparse_shape_and_bad_arguments():
         pa.pa_v2_wave_fit_pages_per_chunk([0, 5], 0, 152)
     with pytest.raises(pa.PaError):
         pa.pa_v2_wave_fit_pages_per_chunk([1, 5], 1, 152)
+
+
+def test_host_graph_rejects_bad_arguments_before_any_cuda_call():
+    import ctypes
+    L = pa.lib()
+    g = ctypes.c_void_p()
+    args = [None] * 6 + [pa.PA_F16, 1, None, None, None, 0.1, None, None]
+    assert L.pa_v2_host_graph_create(None, *args[1:], ctypes.byref(g)) == pa.PA_EINVAL
+    assert L.pa_v2_host_graph_create(None, *args[1:], None) == pa.PA_EINVAL
+    assert not g.value
+    assert L.pa_v2_host_graph_run(None, None) == pa.PA_EINVAL
+    L.pa_v2_host_graph_destroy(None)  # a no-op
