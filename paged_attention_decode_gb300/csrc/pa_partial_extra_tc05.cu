@@ -394,7 +394,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
       // one copy group per block, in the order the blocks are freed (latent blocks 2j, 2j+1 once O^T
       // m-tile j of tile i-1 is done, the extra block, which held P^T, with the last pair); block b is
       // published once the groups issued after it leave at most kTLag groups in flight
-#pragma unroll 1
+      // source rows resolved once per tile; the block loop is unrolled, so the 72 copies issue as
+      // straight-line code (a loop with per-copy 64-bit address arithmetic issued them at about
+      // half the rate, which bounded the kernel)
+      const T* ksrc[8];
+      const T* esrc[8];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int64_t pr = prow[s] >= 0 ? prow[s] : 0;
+        ksrc[s] = kpool + pr * x.k_stride + ch * 8;
+        esrc[s] = epool + pr * x.e_stride + ch * 8;
+      }
+#pragma unroll
       for (int b = 0; b < kTBlocks; ++b) {
         if (i > 0 && (b & 1) == 0 && b < 8 &&
             !wait_phase(&bars[kBarPv + (b >> 1)], (uint32_t)((i - 1) & 1), abort_flag, p.status)) {
@@ -412,9 +423,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
           const int row = rsub + 16 * s;
           const uint32_t dst = dst0 + sw128(row, ch);
           if (prow[s] >= 0) {
-            const T* src = b == 8 ? epool + prow[s] * x.e_stride + ch * 8
-                                  : kpool + prow[s] * x.k_stride + b * 64 + ch * 8;
-            cp_async_16_plain(dst, src);
+            cp_async_16_plain(dst, b == 8 ? esrc[s] : ksrc[s] + b * 64);
           } else {
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
           }
