@@ -71,6 +71,9 @@ def parse_args():
                     help="time the one-launch pa_v2_decode (merge fused into the partial kernel) instead of "
                          "pa_v2_decode_partial + pa_merge_states")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
+    ap.add_argument("--chunking", choices=["search", "wave-fit"], default="search",
+                    help="headline chunk size: pa_v2_plan's own search, or the smallest that fits one wave of the "
+                         "target (pa_v2_wave_fit_pages_per_chunk); the other one is timed beside it")
     ap.add_argument("--dsa-batch", default="1,16", help="dsa_sparse_decode: comma-separated batch sizes")
     ap.add_argument("--profile", type=int, default=0,
                     help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
@@ -309,6 +312,16 @@ def run_ours(args):
                                                          b0.page_size, dt)
     plan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size, b0.num_qo_heads,
                          b0.num_kv_heads, b0.head_dim, dt, target, 0, b0.seq_lens)
+    # the search takes the largest size that still reaches the target, which leaves a short last chunk per
+    # KV head (113 x 18 + 14 pages at 32K); the smallest size that fits the same wave balances the chunks
+    # (108 x 18 + 104) with the same CTA count.  With HBM the bound, the short chunk's early finish leaves
+    # its bandwidth to the others, and the two measure within about 1 %; both are timed (chunking_ab)
+    search_ppc = plan.pages_per_chunk
+    fit_ppc = pa.pa_v2_wave_fit_pages_per_chunk(b0.indptr, plan.q_groups * plan.num_kv_heads, target)
+    alt_ppc = fit_ppc if args.chunking == "search" else search_ppc
+    if args.chunking == "wave-fit" and fit_ppc != plan.pages_per_chunk:
+        plan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size,
+                             b0.num_qo_heads, b0.num_kv_heads, b0.head_dim, dt, target, fit_ppc, b0.seq_lens)
     plan.struct.kernel = args.kernel
     ri, ti, oi = plan.device_arrays(dev)
     sets = [b.to(dev) for b in sets_cpu]
@@ -434,6 +447,13 @@ def run_ours(args):
     stream.synchronize()
     partial_ms = p_start.elapsed_time(p_end) / (reps * G)
 
+    # the chunking choice, measured in this run: the timed step's plan against the other chunking,
+    # alternating graph replays of each (same rotating inputs) so that both see the same clocks
+    chunking_ab = None
+    if alt_ppc and alt_ppc != plan.pages_per_chunk and not args.fused and graph is not None:
+        chunking_ab = compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, graph, G)
+        chunking_ab["alt_chunking"] = "wave-fit" if args.chunking == "search" else "search"
+
     # end to end through the public API with host buffers
     e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
 
@@ -451,6 +471,9 @@ def run_ours(args):
         "config": {"workload": "llama3_8b_32k", "batch": B, "num_qo_heads": Hq, "num_kv_heads": b0.num_kv_heads,
                    "head_dim": D, "page_size": b0.page_size, "context": args.context, "kv_dtype": "f16",
                    "kv_bytes_per_step": kv_bytes, "target_ctas": target, "pages_per_chunk": plan.pages_per_chunk,
+                   "chunking": args.chunking, "search_pages_per_chunk": search_ppc,
+                   "wave_fit_pages_per_chunk": fit_ppc,
+                   "chunking_ab": chunking_ab,
                    "num_chunks": N, "ctas": plan.total_ctas, "merge": bool(plan.needs_merge),
                    "step": STEP_FUSED if args.fused else STEP_TWO,
                    "l2": f"rotating {len(sets)} independent input sets ({len(sets) * kv_bytes >> 20} MiB of K/V "
@@ -471,6 +494,55 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, graph, G, rounds=5):
+    """Median us/step of the timed step's plan and of the plan with `alt_ppc` pages per chunk, from
+    `rounds` alternating timed regions of graph replays (two launches per step, as in the timed step)."""
+    splan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size, b0.num_qo_heads,
+                          b0.num_kv_heads, b0.head_dim, dt, target, alt_ppc, b0.seq_lens)
+    splan.struct.kernel = args.kernel
+    sri, sti, soi = splan.device_arrays(dev)
+    B, Hq, D = b0.batch, b0.num_qo_heads, b0.head_dim
+    swv = torch.empty(splan.num_chunks, Hq, D, device=dev)
+    swl = torch.empty(splan.num_chunks, Hq, device=dev)
+    sout = torch.empty(B, Hq, D, device=dev)
+    slse = torch.empty(B, Hq, device=dev)
+
+    def search_step(i):
+        d = sets[i % len(sets)]
+        pa.pa_v2_decode_partial(splan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                d.first_page_offset, b0.scale, swv, swl, None, stream, sri, sti)
+        if splan.needs_merge:
+            pa.pa_merge_states(swv, swl, soi, B, sout, slse, None, stream)
+
+    sgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(sgraph, stream=stream):
+        for i in range(G):
+            search_step(i)
+    reps = max(1, min(args.steps, 20000) // G)
+
+    def timed(g):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e.record(stream)
+        stream.synchronize()
+        return s.elapsed_time(e) * 1e3 / (reps * G)
+
+    ours, search = [], []
+    for _ in range(rounds):
+        ours.append(timed(graph))
+        search.append(timed(sgraph))
+    med = lambda v: sorted(v)[len(v) // 2]  # noqa: E731
+    return {"us_per_step": med(ours), "alt_us_per_step": med(search), "alt_pages_per_chunk": alt_ppc,
+            "alt_ctas": splan.total_ctas, "alt_num_chunks": splan.num_chunks, "rounds": rounds,
+            "steps_per_round": reps * G}
 
 
 def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
