@@ -71,9 +71,14 @@ def parse_args():
                     help="time the one-launch pa_v2_decode (merge fused into the partial kernel) instead of "
                          "pa_v2_decode_partial + pa_merge_states")
     ap.add_argument("--target", type=int, default=0, help="override the plan's CTA target (0: device-derived)")
-    ap.add_argument("--chunking", choices=["search", "wave-fit"], default="search",
-                    help="headline chunk size: pa_v2_plan's own search, or the smallest that fits one wave of the "
-                         "target (pa_v2_wave_fit_pages_per_chunk); the other one is timed beside it")
+    ap.add_argument("--chunking", choices=["balanced", "search", "wave-fit", "tuned"], default="balanced",
+                    help="headline chunk size: pa_v2_balanced_pages_per_chunk of the plan's own search (same CTA "
+                         "count, equal stage counts for the kernel's warps), the search itself, the smallest size "
+                         "that fits one wave of the target (pa_v2_wave_fit_pages_per_chunk), or the autotuner's "
+                         "pick (autotune.tune, timed launches before the timed region); the search (or, for it, "
+                         "the wave fit) is timed beside it")
+    ap.add_argument("--pages-per-chunk", type=int, default=0,
+                    help="headline: a fixed chunk size instead of --chunking's (the plan's override argument)")
     ap.add_argument("--dsa-batch", default="1,16", help="dsa_sparse_decode: comma-separated batch sizes")
     ap.add_argument("--profile", type=int, default=0,
                     help="profiling mode: run this many eager steps on one input set and exit (no JSON line)")
@@ -312,16 +317,25 @@ def run_ours(args):
                                                          b0.page_size, dt)
     plan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size, b0.num_qo_heads,
                          b0.num_kv_heads, b0.head_dim, dt, target, 0, b0.seq_lens)
-    # the search takes the largest size that still reaches the target, which leaves a short last chunk per
-    # KV head (113 x 18 + 14 pages at 32K); the smallest size that fits the same wave balances the chunks
-    # (108 x 18 + 104) with the same CTA count.  With HBM the bound, the short chunk's early finish leaves
-    # its bandwidth to the others, and the two measure within about 1 %; both are timed (chunking_ab)
+    # the search takes the largest size that still reaches the target (113 pages at 32K: 18 chunks of 113
+    # and one of 14 per KV head); the kernel's 8 warps take a chunk's 16-row stages in turn, so 113 leaves
+    # one warp a 15th stage while 112 gives each 14 with the same CTA count.  The search's size is timed
+    # beside the one used (chunking_ab)
     search_ppc = plan.pages_per_chunk
     fit_ppc = pa.pa_v2_wave_fit_pages_per_chunk(b0.indptr, plan.q_groups * plan.num_kv_heads, target)
-    alt_ppc = fit_ppc if args.chunking == "search" else search_ppc
-    if args.chunking == "wave-fit" and fit_ppc != plan.pages_per_chunk:
+    alt_ppc = fit_ppc if args.chunking == "search" and not args.pages_per_chunk else search_ppc
+    if args.profile and args.chunking == "tuned" and not args.pages_per_chunk:
+        raise SystemExit("bench: --profile runs no autotuning; give --pages-per-chunk (or --chunking search)")
+    tuned = None
+    if args.chunking == "tuned" and not args.pages_per_chunk and not args.profile and args.kernel == 0:
+        from paged_attention_decode_gb300 import autotune
+        tuned = autotune.tune(b0, dev, target_ctas=target, reps=30, fused=args.fused)
+    balanced = pa.pa_v2_balanced_pages_per_chunk(b0.indptr, b0.page_size, search_ppc)
+    fixed = args.pages_per_chunk or {"wave-fit": fit_ppc, "balanced": balanced}.get(args.chunking, 0) or (
+        tuned.pages_per_chunk if tuned else 0)
+    if fixed and fixed != plan.pages_per_chunk:
         plan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size,
-                             b0.num_qo_heads, b0.num_kv_heads, b0.head_dim, dt, target, fit_ppc, b0.seq_lens)
+                             b0.num_qo_heads, b0.num_kv_heads, b0.head_dim, dt, target, fixed, b0.seq_lens)
     plan.struct.kernel = args.kernel
     ri, ti, oi = plan.device_arrays(dev)
     sets = [b.to(dev) for b in sets_cpu]
@@ -447,12 +461,18 @@ def run_ours(args):
     stream.synchronize()
     partial_ms = p_start.elapsed_time(p_end) / (reps * G)
 
+    # per-step distribution: one step at a time after a 512 MiB read that evicts L2, CUDA events around
+    # each replay of a one-step graph (median and p10-p90 of 200 steps after 10 warm-up steps)
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    cold_med, cold_p10, cold_p90 = _time_cold(lambda: step(0), stream, flush, 10, 200, True)
+    del flush
+
     # the chunking choice, measured in this run: the timed step's plan against the other chunking,
     # alternating graph replays of each (same rotating inputs) so that both see the same clocks
     chunking_ab = None
     if alt_ppc and alt_ppc != plan.pages_per_chunk and not args.fused and graph is not None:
         chunking_ab = compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, graph, G)
-        chunking_ab["alt_chunking"] = "wave-fit" if args.chunking == "search" else "search"
+        chunking_ab["alt_chunking"] = "wave-fit" if alt_ppc == fit_ppc and alt_ppc != search_ppc else "search"
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
@@ -471,7 +491,11 @@ def run_ours(args):
         "config": {"workload": "llama3_8b_32k", "batch": B, "num_qo_heads": Hq, "num_kv_heads": b0.num_kv_heads,
                    "head_dim": D, "page_size": b0.page_size, "context": args.context, "kv_dtype": "f16",
                    "kv_bytes_per_step": kv_bytes, "target_ctas": target, "pages_per_chunk": plan.pages_per_chunk,
-                   "chunking": args.chunking, "search_pages_per_chunk": search_ppc,
+                   "chunking": f"fixed {args.pages_per_chunk}" if args.pages_per_chunk else args.chunking,
+                   "search_pages_per_chunk": search_ppc, "balanced_pages_per_chunk": balanced,
+                   "autotune": None if tuned is None else {
+                       "reps": 30, "protocol": "each candidate: median of 30 steps, 512 MiB read before each",
+                       "times_us": {str(k): round(v, 2) for k, v in sorted(tuned.times_us.items())}},
                    "wave_fit_pages_per_chunk": fit_ppc,
                    "chunking_ab": chunking_ab,
                    "num_chunks": N, "ctas": plan.total_ctas, "merge": bool(plan.needs_merge),
@@ -485,6 +509,9 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": partial_bytes, "launch_us": partial_ms * 1e3,
                      "rest_of_step_us": ms_step * 1e3 - partial_ms * 1e3,
                      "peak_source": f"{peak_kind} hbm_gbs"},
+        "per_step_cold_l2": {"median_us": cold_med, "p10_us": cold_p10, "p90_us": cold_p90, "steps": 200,
+                             "protocol": "512 MiB read before each step; CUDA events around one graph replay "
+                                         "of the step"},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,

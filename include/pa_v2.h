@@ -158,9 +158,6 @@ pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len,
                      int32_t* kv_tile_indices, int32_t cap_chunks, int32_t* o_indptr,
                      pa_v2_plan_t* out);
 
-/* 1 if `plan` is still valid for this geometry (same batch and per-request
- * page counts, and a geometry that passes the checks of pa_v2_plan); else 0.
- * Host pointers. */
 /* The smallest pages_per_chunk whose CTA count -- sum over requests of
  * max(1, ceil(pages_r / ppc)) * ctas_per_chunk, pages_r = indptr[r+1] -
  * indptr[r] -- is at most `wave`; pass it to pa_v2_plan as
@@ -172,6 +169,23 @@ pa_status pa_v2_plan(const int32_t* indptr, const int32_t* last_page_len,
 int32_t pa_v2_wave_fit_pages_per_chunk(const int32_t* indptr, int32_t batch, int32_t ctas_per_chunk,
                                        int32_t wave);
 
+/* A pages_per_chunk at or below `pages_per_chunk` (normally the plan's own
+ * choice) with the same chunk count -- sum over requests of
+ * max(1, ceil(pages_r / ppc)) -- whose chunks give each of the 8 warps of the
+ * tensor-core partial kernel the same number of stages (a stage is 16 pool
+ * rows: floor(16 / page_size) pages, or a 16-row slice of a page when
+ * page_size is a multiple of 16); the largest such size, else
+ * `pages_per_chunk` itself (also for page sizes above 16 that are not
+ * multiples of 16).  A launch ends with its busiest warp: at 32768 tokens of
+ * 16-row pages, 112 pages per chunk (14 stages per warp) against the search's
+ * 113 (one warp with 15).  Pass the result to pa_v2_plan as
+ * pages_per_chunk_override.  0 for bad arguments.  Host pointers. */
+int32_t pa_v2_balanced_pages_per_chunk(const int32_t* indptr, int32_t batch, int32_t page_size,
+                                       int32_t pages_per_chunk);
+
+/* 1 if `plan` is still valid for this geometry (same batch and per-request
+ * page counts, and a geometry that passes the checks of pa_v2_plan); else 0.
+ * Host pointers. */
 int32_t pa_v2_plan_matches(const pa_v2_plan_t* plan, const int32_t* indptr,
                            const int32_t* last_page_len, const int32_t* first_page_offset,
                            int32_t batch);

@@ -219,6 +219,49 @@ int32_t pa_v2_wave_fit_pages_per_chunk(const int32_t* indptr, int32_t batch, int
   return lo;
 }
 
+// A chunk size that gives every warp of the tensor-core partial kernel the same
+// number of stages.  That kernel stages 16 pool rows at a time -- floor(16 /
+// page_size) whole pages when page_size <= 16, a 16-row slice of a page when
+// page_size is a multiple of 16 -- and its 8 warps take a chunk's stages in
+// turn, so a launch ends with the busiest warp: at 32768 tokens of 16-row pages
+// the plan's 113 pages per chunk leave one warp a 15th stage, 112 = 8 x 14 do
+// not.  Scans down from `pages_per_chunk` for the largest size whose stage
+// count is a multiple of 8 and whose chunk count (sum over requests of
+// max(1, ceil(pages_r / size))) is still that of `pages_per_chunk`.
+constexpr int32_t kBalanceStageRows = 16;  // rows per stage (pa_internal.cuh kStageRows)
+constexpr int32_t kBalanceWarps = 8;       // warps per CTA of the tensor-core kernel
+
+int32_t pa_v2_balanced_pages_per_chunk(const int32_t* indptr, int32_t batch, int32_t page_size,
+                                       int32_t pages_per_chunk) {
+  if (!indptr || batch < 1 || page_size < 1 || pages_per_chunk < 1 || indptr[0] != 0) return 0;
+  for (int32_t r = 0; r < batch; ++r)
+    if (indptr[r + 1] < indptr[r]) return 0;
+  if (page_size > kBalanceStageRows && page_size % kBalanceStageRows != 0) return pages_per_chunk;
+  auto stages = [&](int64_t size) -> int64_t {
+    if (page_size <= kBalanceStageRows) {
+      const int64_t per = kBalanceStageRows / page_size;
+      return (size + per - 1) / per;
+    }
+    return size * (page_size / kBalanceStageRows);
+  };
+  auto chunks = [&](int64_t size) {
+    int64_t n = 0;
+    for (int32_t r = 0; r < batch; ++r) {
+      const int64_t pages = indptr[r + 1] - indptr[r];
+      n += pages <= size ? 1 : (pages + size - 1) / size;
+    }
+    return n;
+  };
+  const int64_t want = chunks(pages_per_chunk);
+  // the chunk count does not decrease as the size shrinks: stop at the first size that adds a chunk
+  for (int64_t size = pages_per_chunk; size >= 1; --size) {
+    if (stages(size) % kBalanceWarps != 0) continue;
+    if (chunks(size) != want) break;
+    return static_cast<int32_t>(size);
+  }
+  return pages_per_chunk;
+}
+
 const char* pa_version(void) { return "pa_v2 0.1 (sm_103a)"; }
 
 }  // extern "C"

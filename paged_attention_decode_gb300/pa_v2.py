@@ -35,7 +35,7 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
                "pa_v2_decode_partial_extra", "pa_v2_selftest_wait", "pa_v2_host_graph_create",
                "pa_v2_host_graph_run", "pa_v2_host_graph_destroy", "pa_v2_wave_fit_pages_per_chunk",
-               "pa_status_from_device", "pa_status_string", "pa_version")
+               "pa_v2_balanced_pages_per_chunk", "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_host_graph_destroy.restype = None
         L.pa_v2_wave_fit_pages_per_chunk.argtypes = [P, i32, i32, i32]
         L.pa_v2_wave_fit_pages_per_chunk.restype = i32
+        L.pa_v2_balanced_pages_per_chunk.argtypes = [P, i32, i32, i32]
+        L.pa_v2_balanced_pages_per_chunk.restype = i32
         L.pa_selection_rows_per_request.argtypes = [i32, i32, i32]
         L.pa_selection_rows_per_request.restype = i64
         L.pa_sparse_csr.argtypes = [i32, i64, P, P, P]
@@ -635,4 +637,15 @@ def pa_v2_wave_fit_pages_per_chunk(indptr, ctas_per_chunk: int, wave: int) -> in
     v = int(lib().pa_v2_wave_fit_pages_per_chunk(ip.data_ptr(), ip.numel() - 1, int(ctas_per_chunk), int(wave)))
     if v <= 0:
         raise PaError(PA_EINVAL, "pa_v2_wave_fit_pages_per_chunk")
+    return v
+
+
+def pa_v2_balanced_pages_per_chunk(indptr, page_size: int, pages_per_chunk: int) -> int:
+    """Largest pages_per_chunk <= the given one with its chunk count whose chunks give the tensor-core
+    kernel's 8 warps equal stage counts, else the given one (pa_v2_balanced_pages_per_chunk); host indptr."""
+    ip = torch.as_tensor(indptr, dtype=torch.int32).contiguous()
+    v = int(lib().pa_v2_balanced_pages_per_chunk(ip.data_ptr(), ip.numel() - 1, int(page_size),
+                                                 int(pages_per_chunk)))
+    if v <= 0:
+        raise PaError(PA_EINVAL, "pa_v2_balanced_pages_per_chunk")
     return v

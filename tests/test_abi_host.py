@@ -266,6 +266,46 @@ def test_wave_fit_on_the_sparse_shape_and_bad_arguments():
         pa.pa_v2_wave_fit_pages_per_chunk([1, 5], 1, 152)
 
 
+def _stages(size, ps):
+    return -(-size // (16 // ps)) if ps <= 16 else size * (ps // 16)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_balanced_size_brute_force(seed):
+    """Brute force: the result keeps the given size's chunk count, gives a stage count that is a multiple of
+    8 (the tensor-core kernel's warps), and no larger size up to the given one does both; when no size
+    does, the given size comes back."""
+    import random
+    rng = random.Random(100 + seed)
+    pages = [rng.choice([0, 1, 5, 113, 2048, rng.randint(0, 3000)]) for _ in range(rng.randint(1, 6))]
+    indptr = [0]
+    for p in pages:
+        indptr.append(indptr[-1] + p)
+    for ps in (1, 2, 4, 8, 16, 32, 64):
+        for ppc in sorted({1, 7, 8, 57, 113, 228, rng.randint(1, 3000)}):
+            got = pa.pa_v2_balanced_pages_per_chunk(indptr, ps, ppc)
+            want = _ctas(pages, ppc, 1)
+            ok = [s for s in range(1, ppc + 1) if _stages(s, ps) % 8 == 0 and _ctas(pages, s, 1) == want]
+            assert got == (max(ok) if ok else ppc), (pages, ps, ppc)
+
+
+def test_balanced_size_on_the_32k_decode_and_bad_arguments():
+    # 2048 pages of 16 rows: the plan's 113 pages per chunk make 19 chunks with 113 stages each (one warp
+    # of 8 takes 15); 112 keeps 19 chunks at 14 stages per warp
+    assert pa.pa_v2_balanced_pages_per_chunk([0, 2048], 16, 113) == 112
+    assert pa.pa_v2_balanced_pages_per_chunk([0, 2048], 16, 112) == 112
+    # 16 requests of 2048 one-row pages at 228 pages (15 stages of 16 pages): 8 stages would need 9 -> 16
+    # chunks per request, so the size stays
+    assert pa.pa_v2_balanced_pages_per_chunk([2048 * r for r in range(17)], 1, 228) == 228
+    # 64-row pages: 4 stages per page, any even size balances
+    assert pa.pa_v2_balanced_pages_per_chunk([0, 1000], 64, 101) == 100
+    # page sizes above 16 that are not multiples of 16 are left alone
+    assert pa.pa_v2_balanced_pages_per_chunk([0, 1000], 24, 101) == 101
+    for bad in (([0, 5], 0, 3), ([0, 5], 16, 0), ([1, 5], 16, 3), ([0, 5, 4], 16, 3)):
+        with pytest.raises(pa.PaError):
+            pa.pa_v2_balanced_pages_per_chunk(*bad)
+
+
 def test_host_graph_rejects_bad_arguments_before_any_cuda_call():
     import ctypes
     L = pa.lib()

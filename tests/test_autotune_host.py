@@ -21,3 +21,17 @@ def test_wave_fit_is_the_smallest_size_within_k_waves():
     assert {108, 54, 36} <= set(c)
     for ppc, waves in ((108, 1), (54, 2), (36, 3)):
         assert T._chunks([2048], ppc) * 8 <= waves * 152 < T._chunks([2048], ppc - 1) * 8
+
+
+def test_sizes_below_the_default_with_its_cta_count():
+    # 32768 tokens of 16-token pages, 8 KV heads: the default 113 pages makes 19 chunks; so does every
+    # size down to 108 (ceil(2048 / 107) = 20), and those five are candidates -- 112 = 8 x 14 among them
+    indptr = torch.tensor([0, 2048])
+    c = T.candidates(indptr, 8, 1, 152, 113, 1, 2048)
+    assert {108, 109, 110, 111, 112, 113} <= set(c) and 107 not in c
+    for ppc in range(108, 114):
+        assert T._chunks([2048], ppc) == 19
+    assert T._chunks([2048], 107) == 20
+    # at most `same_ctas` of them
+    c3 = T.candidates(indptr, 8, 1, 152, 113, 1, 2048, same_ctas=3)
+    assert {110, 111, 112} <= set(c3) and 109 not in c3
