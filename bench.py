@@ -693,6 +693,7 @@ def run_workload(args):
 
     d = b.to(dev)
     plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, b.ppc_override)
+    search_ppc0 = plan.pages_per_chunk
     chunking = "fixed by the workload" if b.ppc_override else "pa_v2_plan's search"
     wave = pa.pa_v2_default_target_ctas(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, dt)
     if not b.ppc_override and not cascade and plan.total_ctas > wave:
@@ -700,6 +701,15 @@ def run_workload(args):
         fit = pa.pa_v2_wave_fit_pages_per_chunk(b.indptr, plan.q_groups * plan.num_kv_heads, wave)
         plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, fit)
         chunking = "pa_v2_wave_fit_pages_per_chunk (the search's size spilled past one wave)"
+    search_plan = None
+    if not b.ppc_override and not cascade and not args.tune and plan.total_ctas <= wave:
+        # the largest size at or below the search's with its chunk count that gives the kernel's 8 warps
+        # equal stage counts; the search's own plan is timed beside it ("two_search")
+        bal = pa.pa_v2_balanced_pages_per_chunk(b.indptr, b.page_size, plan.pages_per_chunk)
+        if bal != plan.pages_per_chunk:
+            search_plan = plan
+            plan = make_plan(b.indptr, b.last_page_len, b.first_page_offset, b.num_qo_heads, b.seq_lens, bal)
+            chunking = "pa_v2_balanced_pages_per_chunk of the search's size (equal stage counts per warp)"
     tuned = None
     if args.tune and not cascade:
         from paged_attention_decode_gb300 import autotune
@@ -732,6 +742,18 @@ def run_workload(args):
                                     d.first_page_offset, b.scale, out, lse, None, stream)
 
     steps = {"two": (two_step, b.kv_bytes()), "fused": (flat_step, b.kv_bytes())}
+    if search_plan is not None:
+        s_ws = workspace(search_plan)
+        s_oi = search_plan.device_arrays(dev)[2]
+        s_out = torch.empty_like(out)
+        s_lse = torch.empty_like(lse)
+
+        def two_search_step():
+            pa.pa_v2_decode_partial(search_plan, d.q, d.k_pool, d.v_pool, d.indices, d.indptr, d.last_page_len,
+                                    d.first_page_offset, b.scale, s_ws[0], s_ws[1], None, stream)
+            pa.pa_merge_states(s_ws[0], s_ws[1], s_oi, b.batch, s_out, s_lse, None, stream)
+
+        steps["two_search"] = (two_search_step, b.kv_bytes())
     if cascade:
         from paged_attention_decode_gb300 import cascade as C
         M, Hq, D = b.q.shape
@@ -774,6 +796,13 @@ def run_workload(args):
         err = float(abs(out.cpu().double().numpy() - ref_o).max())
         if not err <= 2e-3:
             raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}); refusing to time")
+    if search_plan is not None:
+        with torch.cuda.stream(stream):
+            steps["two_search"][0]()
+        stream.synchronize()
+        err = float(abs(s_out.cpu().double().numpy() - ref_o).max())
+        if not err <= 2e-3:
+            raise SystemExit(f"bench: two_search output disagrees with the oracle ({err:.3e}); refusing to time")
     if cascade:
         with torch.cuda.stream(stream):
             steps["cascade"][0]()
@@ -821,6 +850,7 @@ def run_workload(args):
                        "kv_dtype": str(b.dtype).replace("torch.", ""), "seq_lens_total": sum(b.seq_lens),
                        "num_chunks": plan.num_chunks, "pages_per_chunk": plan.pages_per_chunk,
                        "chunking": chunking,
+                       "search_pages_per_chunk": search_ppc0,
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
     if tuned is not None:
