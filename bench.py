@@ -941,6 +941,16 @@ def run_block_sparse(args):
     def block_granular():
         pa.decode(plan2, d.q, kp2, vp2, pages_d, ip2d, lp2d, fp2d, s.scale, out2, lse2, ws2, None, stream)
 
+    if args.profile:
+        with torch.cuda.stream(stream):
+            for _ in range(args.profile):
+                token_exact()
+                block_granular()
+        stream.synchronize()
+        print(f"profile mode: block_sparse_selection, {args.profile} steps of [token_exact, block_granular]",
+              flush=True)
+        return
+
     # correctness guard against the oracle before timing
     ref_rows, _ = oracle.selection_rows_ref(s.block_ids, C, s.kv_len, s.cap)
     ref_o, _ = oracle.attention(s.q, s.k_pool, s.v_pool, ref_rows, ip, lp, fp, s.scale)
