@@ -68,6 +68,22 @@ def test_sliding_window_batch():
     check_batch(W.sliding_window_batch())
 
 
+@pytest.mark.parametrize("name", ["sliding_window_batch", "sparse_token_exact"])
+def test_balanced_chunk_size_is_exact(name):
+    """The chunk size bench.py takes for the paged workloads when the plan's search fits one wave:
+    pa_v2_balanced_pages_per_chunk of the search's (72 for the sliding-window batch, the search's own
+    228 for the sparse decode's one-wave fit), partials and merged output against the oracle."""
+    b = W.WORKLOADS[name]()
+    search = make_plan(b)
+    ppc = search.pages_per_chunk
+    if search.total_ctas > search.target_ctas:
+        ppc = pa.pa_v2_wave_fit_pages_per_chunk(b.indptr, search.q_groups * search.num_kv_heads,
+                                                search.target_ctas)
+    bal = pa.pa_v2_balanced_pages_per_chunk(b.indptr, b.page_size, ppc)
+    plan, *_ = check_batch(b, override=bal, fused=False)
+    assert plan.num_chunks == make_plan(b, override=ppc).num_chunks
+
+
 def test_sparse_token_exact_full():
     b = W.sparse_token_exact()
     check_batch(b)
