@@ -43,6 +43,7 @@ METRIC = "decode KV-read GB/s (% of GB300 HBM peak) and µs/step at 32K context"
 STEP_TWO = "pa_v2_decode_partial + pa_merge_states (merge launched as a programmatic dependent)"
 STEP_FUSED = "pa_v2_decode (merge fused into the partial kernel)"
 FALLBACK_HBM_GBS = 6800.0
+DELAY_CYCLES = 400_000   # device-side delay before the start event (about 200 us at 2 GHz)
 
 
 def parse_args():
@@ -56,6 +57,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip timing the other four workloads")
     ap.add_argument("--context", type=int, default=32768)
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix",
@@ -387,52 +389,69 @@ def run_ours(args):
     if err > 2e-3:
         raise SystemExit(f"bench: GPU output disagrees with the oracle (max|d| = {err:.3e}); refusing to time")
 
-    graph = None
-    G = len(sets) * 10
-    if args.graph:
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                step(i)
-        stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(G):
-                step(i)
-
-    def run_steps(k, start=0):
-        if graph is None:
-            with torch.cuda.stream(stream):
-                for i in range(k):
-                    step(start + i)
-            return
-        full, rem = divmod(k, G)
-        with torch.cuda.stream(stream):
-            for _ in range(full):
-                graph.replay()
-            for i in range(rem):
-                step(i)
-
-    # warmup
-    run_steps(args.warmup)
+    # The timed steps replay CUDA graphs that hold exactly those steps: one graph of min(K, 600) steps
+    # (600 is a multiple of the 3-set rotation, so the rotation continues across replays) replayed
+    # K // 600 times, plus one graph of the remaining steps.  Each graph is replayed once untimed after the
+    # warm-up steps, so its upload is not timed.
+    graphs = []
+    G = len(sets) * 10   # steps per graph of the side measurements (partial-only, chunking A/B)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
     stream.synchronize()
+    if args.graph:
+        per = min(args.steps, 200 * len(sets))
+        full, rem = divmod(args.steps, per)
+        for n_steps, start, times in ((per, 0, full), (rem, full * per, 1 if rem else 0)):
+            if times == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n_steps):
+                    step(start + i)
+            graphs.append((g, n_steps, times))
 
-    # timed region
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+    def run_steps(k, start=0, timed=False):
+        if timed and graphs:
+            with torch.cuda.stream(stream):
+                for g, _, times in graphs:
+                    for _ in range(times):
+                        g.replay()
+            return
+        with torch.cuda.stream(stream):
+            for i in range(k):
+                step(start + i)
+
+    # Timed region.  nvidia-smi samples clocks from before the warm-up until after the timed steps, so its
+    # start-up does not fall between them.  Warm-up: W steps, then one untimed replay of each timed graph
+    # (its upload).  After the barrier and synchronisation, a device-side delay queued before the start
+    # event (torch.cuda._sleep: the SM spins for DELAY_CYCLES clocks, about 200 us) gives the host time to
+    # enqueue the timed graph replays, so the events time the steps back to back on the device rather than
+    # the host's enqueue latency.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        run_steps(args.warmup)
+        with torch.cuda.stream(stream):
+            for g, _, _ in graphs:
+                g.replay()
+        stream.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         clocks.mark("start")
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(DELAY_CYCLES)
         t_start.record(stream)
-        run_steps(args.steps)
+        run_steps(args.steps, timed=True)
         t_end.record(stream)
         stream.synchronize()
         clocks.mark("end")
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
+    untimed_graph_steps = sum(n for _, n, _ in graphs)
     ms_total, job_bytes = reduce_over_ranks(t_start.elapsed_time(t_end), float(kv_bytes) * args.steps, world, dev)
     ms_step = ms_total / args.steps
 
@@ -470,14 +489,31 @@ def run_ours(args):
     # the chunking choice, measured in this run: the timed step's plan against the other chunking,
     # alternating graph replays of each (same rotating inputs) so that both see the same clocks
     chunking_ab = None
-    if alt_ppc and alt_ppc != plan.pages_per_chunk and not args.fused and graph is not None:
-        chunking_ab = compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, graph, G)
+    if alt_ppc and alt_ppc != plan.pages_per_chunk and not args.fused and args.graph:
+        chunking_ab = compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, step, G)
         chunking_ab["alt_chunking"] = "wave-fit" if alt_ppc == fit_ppc and alt_ppc != search_ppc else "search"
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0)
 
+    # the other four workloads, each checked against the oracle before it is timed
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {"llama3_8b_32k": {
+            "us_per_step": ms_step * 1e3, "protocol": "the timed steps above (graph replays, rotating sets)",
+            "cold_l2_median_us": cold_med, "kv_bytes_per_step": kv_bytes,
+            "kv_read_gbs": kv_bytes / (ms_step * 1e-3) / 1e9,
+            "pct_of_hbm_peak": 100.0 * kv_bytes / (ms_step * 1e-3) / 1e9 / measured_peak()[0],
+            "oracle_check": {"max_abs_out": err}}}
+        per_config.update(other_configs(args))
+
     peak, peak_kind = measured_peak()
+    timed_protocol = ({"timed_replays": sum(t for _, _, t in graphs),
+                       "steps_per_graph": [n for _, n, _ in graphs],
+                       "untimed_upload_replay_steps": untimed_graph_steps,
+                       "start": f"after a {DELAY_CYCLES}-cycle device-side delay (torch.cuda._sleep) queued after "
+                                "the synchronisation, so the replays are enqueued before the start event"}
+                      if graphs else False)
     gbs = job_bytes / (ms_total * 1e-3) / 1e9
     achieved = partial_bytes / (partial_ms * 1e-3) / 1e9
     kernel_name = "pa_v2_partial_simt_kernel" if args.kernel == 1 else "pa_v2_partial_tc_kernel"
@@ -487,7 +523,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
         "pct_of_hbm_peak": 100.0 * gbs / world / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
         "pct_of_nominal_8tbs": 100.0 * gbs / world / 8000.0,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": "llama3_8b_32k", "batch": B, "num_qo_heads": Hq, "num_kv_heads": b0.num_kv_heads,
                    "head_dim": D, "page_size": b0.page_size, "context": args.context, "kv_dtype": "f16",
                    "kv_bytes_per_step": kv_bytes, "target_ctas": target, "pages_per_chunk": plan.pages_per_chunk,
@@ -502,7 +538,7 @@ def run_ours(args):
                    "step": STEP_FUSED if args.fused else STEP_TWO,
                    "l2": f"rotating {len(sets)} independent input sets ({len(sets) * kv_bytes >> 20} MiB of K/V "
                          "between reuses of a set; L2 is 126 MB)",
-                   "cuda_graph": bool(graph is not None), "parallelism": f"replicas x{world}"},
+                   "cuda_graph": timed_protocol, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
                      "kernel": kernel_name, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
@@ -512,6 +548,7 @@ def run_ours(args):
         "per_step_cold_l2": {"median_us": cold_med, "p10_us": cold_p10, "p90_us": cold_p90, "steps": 200,
                              "protocol": "512 MiB read before each step; CUDA events around one graph replay "
                                          "of the step"},
+        "per_config": per_config,
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
@@ -523,7 +560,35 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, graph, G, rounds=5):
+PER_CONFIG = ("tiny_csr", "sliding_window_batch", "sparse_token_exact", "cascade_shared_prefix")
+
+
+def other_configs(args):
+    """us/step and KV-read GB/s of the other four workloads, each one step at a time after a 512 MiB read
+    (cold L2), median of 100 graph-replayed steps, each arm checked against the oracle first; the cascade
+    workload reports the cascade and the flat launch of the same batch."""
+    res = {}
+    for name in PER_CONFIG:
+        ns = argparse.Namespace(**vars(args))
+        ns.workload, ns.steps, ns.warmup, ns.tune, ns.profile, ns.graph = name, 100, 10, False, 0, 1
+        line = measure_workload(ns)
+        arms = line["arms"]
+        main = "cascade" if name == "cascade_shared_prefix" else "two"
+        entry = {"us_per_step": arms[main]["us_per_step_median"], "p10_us": arms[main]["us_p10"],
+                 "p90_us": arms[main]["us_p90"], "kv_bytes_per_step": arms[main]["kv_bytes_per_step"],
+                 "kv_read_gbs": arms[main]["kv_read_gbs"], "pct_of_hbm_peak": line["pct_of_hbm_peak"],
+                 "pages_per_chunk": line["config"]["pages_per_chunk"], "num_chunks": line["config"]["num_chunks"],
+                 "protocol": "cold L2 (512 MiB read before each step), one graph replay per step, median of 100",
+                 "oracle_check": line["oracle_check"]}
+        if name == "cascade_shared_prefix":
+            entry["flat_us_per_step"] = arms["two"]["us_per_step_median"]
+            entry["flat_logical_kv_bytes_per_step"] = arms["two"]["kv_bytes_per_step"]
+            entry["cascade_over_flat"] = arms["cascade"]["us_per_step_median"] / arms["two"]["us_per_step_median"]
+        res[name] = entry
+    return res
+
+
+def compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, step, G, rounds=5):
     """Median us/step of the timed step's plan and of the plan with `alt_ppc` pages per chunk, from
     `rounds` alternating timed regions of graph replays (two launches per step, as in the timed step)."""
     splan = pa.pa_v2_plan(b0.indptr, b0.last_page_len, b0.first_page_offset, b0.page_size, b0.num_qo_heads,
@@ -543,6 +608,10 @@ def compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, grap
         if splan.needs_merge:
             pa.pa_merge_states(swv, swl, soi, B, sout, slse, None, stream)
 
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            step(i)
     sgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(sgraph, stream=stream):
         for i in range(G):
@@ -666,6 +735,12 @@ def run_e2e_fused(args, pa, plan, sets_cpu, sets, dev, stream, b0):
 
 
 def run_workload(args):
+    line = measure_workload(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def measure_workload(args):
     """Per-step timing of one of the other workloads: every step starts with a cold L2 (a 512 MiB
     buffer is read between steps, outside the event pair).  Arms: "two" = pa_v2_decode_partial +
     pa_merge_states (the default step, `value`), "fused" = the one-launch pa_v2_decode; the cascade adds
@@ -783,33 +858,35 @@ def run_workload(args):
                     fn()
         stream.synchronize()
         print(f"profile mode: {args.workload}, {args.profile} steps of {list(steps)}", flush=True)
-        return
+        return None
 
-    # correctness guard before timing
-    ref_o, _ = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
-                                b.first_page_offset, b.scale)
-    for name in ("two", "fused"):
-        out.fill_(float("nan"))
+    # correctness guard before timing: every arm against the f64 oracle (max |out - oracle|, and
+    # max |lse2 - oracle| where the arm writes the final lse2)
+    ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                    b.first_page_offset, b.scale)
+    oracle_check = {}
+
+    def check(name, o_t, l_t):
         with torch.cuda.stream(stream):
+            o_t.fill_(float("nan"))
+            l_t.fill_(float("nan"))
             steps[name][0]()
         stream.synchronize()
-        err = float(abs(out.cpu().double().numpy() - ref_o).max())
-        if not err <= 2e-3:
-            raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}); refusing to time")
+        err = float(abs(o_t.cpu().double().numpy() - ref_o).max())
+        lg, lr = l_t.cpu().double().numpy(), ref_l
+        fin = lr > -float("inf")
+        lerr = float(abs(lg[fin] - lr[fin]).max()) if fin.any() else 0.0
+        if not (err <= 2e-3 and lerr <= 1e-3 and bool(((lg > -float("inf")) == fin).all())):
+            raise SystemExit(f"bench: {name} output disagrees with the oracle ({err:.3e}, lse2 {lerr:.3e}); "
+                             "refusing to time")
+        oracle_check[name] = {"max_abs_out": err, "max_abs_lse2": lerr}
+
+    check("two", out, lse)
+    check("fused", out, lse)
     if search_plan is not None:
-        with torch.cuda.stream(stream):
-            steps["two_search"][0]()
-        stream.synchronize()
-        err = float(abs(s_out.cpu().double().numpy() - ref_o).max())
-        if not err <= 2e-3:
-            raise SystemExit(f"bench: two_search output disagrees with the oracle ({err:.3e}); refusing to time")
+        check("two_search", s_out, s_lse)
     if cascade:
-        with torch.cuda.stream(stream):
-            steps["cascade"][0]()
-        stream.synchronize()
-        err = float(abs(c_out.cpu().double().numpy() - ref_o).max())
-        if not err <= 2e-3:
-            raise SystemExit(f"bench: cascade output disagrees with the oracle ({err:.3e}); refusing to time")
+        check("cascade", c_out, c_lse)
 
     res = {}
     for name, (fn, nbytes) in steps.items():
@@ -844,7 +921,7 @@ def run_workload(args):
     main = res["cascade" if cascade else "two"]
     line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main["us_per_step_median"],
             "unit": "us/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": {"float16": "f16", "bfloat16": "bf16", "float32": "f32"}[str(b.dtype).replace("torch.", "")], "data": "synthetic",
             "config": {"workload": args.workload, "batch": b.batch, "num_qo_heads": b.num_qo_heads,
                        "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
                        "kv_dtype": str(b.dtype).replace("torch.", ""), "seq_lens_total": sum(b.seq_lens),
@@ -852,12 +929,13 @@ def run_workload(args):
                        "chunking": chunking,
                        "search_pages_per_chunk": search_ppc0,
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
-            "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak}
+            "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak,
+            "oracle_check": oracle_check}
     if tuned is not None:
         line["autotune"] = {"pages_per_chunk": tuned.pages_per_chunk, "default": tuned.default_pages_per_chunk,
                             "times_us": {str(k): round(v, 2) for k, v in tuned.times_us.items()},
                             "num_chunks": {str(k): v for k, v in tuned.num_chunks.items()}}
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def _time_cold(fn, stream, flush, warmup, steps, graph):
@@ -975,7 +1053,7 @@ def run_block_sparse(args):
     main_arm = res["token_exact"]
     line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main_arm["us_per_step_median"],
             "unit": "us/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "f16", "data": "synthetic",
             "config": {"workload": "block_sparse_selection", "requests": R, "num_qo_heads_per_request": n_rep,
                        "head_dim": D, "block_size": C, "topk_blocks": topk, "kv_len": s.kv_len, "cap": s.cap,
                        "rows_per_request": per, "kv_dtype": "float16", "l2": "512 MiB buffer read between steps",
@@ -1166,7 +1244,7 @@ def run_dsa(args):
                         "the MMAs issued are twice that (q and P as hi + lo halves)"}
     line = {"metric": "DSA decode us/step (median, cold L2), KV-read GB/s and TFLOP/s", "unit": "us/step",
             "value": cells[0]["us_per_step_median"], "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+            "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "dsa_sparse_decode", "num_qo_heads": 128, "num_kv_heads": 1, "dim": 512,
                        "extra_dim": 64, "row_stride": 640, "kv_dtype": "bfloat16", "page_size": 1,
                        "kernel": ["pa_v2_partial_extra_tc05_kernel", "pa_v2_partial_extra_kernel",

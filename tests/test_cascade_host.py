@@ -71,6 +71,25 @@ def test_detect_rules_by_hand():
     assert pa.pa_v2_cascade_detect(ip2, idx2, [0, 0], 1, 2)[1] == 19
 
 
+def test_detect_tie_goes_to_the_group_met_first():
+    # two groups remove the same number of page reads: the one keyed by page 50 (requests 0, 2, 4, three
+    # shared pages: 3 x 2 = 6) and the one keyed by page 10 (requests 1, 3, six shared pages: 6 x 1 = 6).
+    # The pages name the larger saving the winner and say nothing of a tie; the reading taken is that the
+    # group whose first member comes first in the batch wins.  Reordering the batch flips the winner.
+    g50 = [[50, 51, 52, 60, 61], [50, 51, 52, 80], [50, 51, 52, 95]]
+    g10 = [list(range(10, 16)) + [70], list(range(10, 16)) + [90, 91]]
+    for tables, want in (([g50[0], g10[0], g50[1], g10[1], g50[2]], ([0, 2, 4], 3)),
+                         ([g10[0], g50[0], g10[1], g50[1], g50[2]], ([0, 2], 6))):
+        indptr = [0]
+        for x in tables:
+            indptr.append(indptr[-1] + len(x))
+        indices = [p for x in tables for p in x]
+        fpo = [0] * len(tables)
+        assert oracle.cascade_detect_ref(indptr, indices, fpo, 1, 2) == want
+        flags, shared = pa.pa_v2_cascade_detect(indptr, indices, fpo, 1, 2)
+        assert ([r for r in range(len(tables)) if int(flags[r])], shared) == want
+
+
 def test_split_rebuilds_the_flat_tables():
     rng = random.Random(9)
     for case in range(100):
