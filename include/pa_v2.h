@@ -446,13 +446,20 @@ void pa_v2_host_graph_destroy(pa_v2_host_graph_t* graph);
  * from a fixed array in the library's own device memory
  * (PA_V2_NOALLOC_SCRATCH_BYTES, laid out as counters, then workspace_v, then
  * workspace_lse, each rounded up to 256 bytes).  It allocates nothing.
- *  - The caller still passes every input and output (same arguments and
- *    layouts as pa_v2_decode, minus workspace_v / workspace_lse / counters).
+ *  - The caller still passes every input and output: the same arguments and
+ *    layouts as pa_v2_decode, minus workspace_v / workspace_lse / counters
+ *    and minus the row maps member_rows / out_rows, which are taken as null:
+ *    request r writes output row r * plan->out_row_step, and member m of a
+ *    stacked plan reads q row group m and writes row m * plan->out_row_step.
  *  - A plan whose counters plus workspace exceed PA_V2_NOALLOC_SCRATCH_BYTES
- *    is rejected with PA_ECAPACITY before anything is launched.
+ *    is rejected with PA_ECAPACITY before anything is launched.  A plan with
+ *    no chunks (batch 0) returns PA_OK and launches nothing.
  *  - The first call on a device looks up that device's copy of the array
- *    (cudaGetSymbolAddress, with that device current) and remembers it; make
- *    that first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and remembers it for
+ *    the life of the process; make that first call before any stream capture.
+ *    The remembered address does not survive cudaDeviceReset: do not call
+ *    this entry point on a device after resetting it.  If the lookup fails
+ *    the call returns PA_ECUDA and clears the runtime's last error.
  *  - Every call on a device shares the one array and leaves its contents
  *    behind.  Each call clears the counter region on its stream
  *    (cudaMemsetAsync) before the launch.  Calls whose work overlaps on the GPU

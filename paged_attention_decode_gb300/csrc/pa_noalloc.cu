@@ -12,7 +12,8 @@
 // loads the library, held until the process exits.  Host code cannot use the
 // array's name as a device address (on the host it names a stand-in), so the
 // first call on each device asks the runtime for that device's address with
-// the device current, and remembers it.
+// the device current, and remembers it for the life of the process (so the
+// address is stale after a cudaDeviceReset of that device).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,7 +39,10 @@ void* scratch_on(int device) {
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[device]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();  // leave no sticky-looking error behind for the caller's next check
+      return nullptr;
+    }
     addr[device] = p;
   }
   return addr[device];

@@ -394,15 +394,24 @@ def pa_v2_decode_noalloc(plan: Plan, q, k_pool, v_pool, indices, indptr, last_pa
 
     The partial workspace and the ticket counters come from the library's own fixed device array
     (NOALLOC_SCRATCH_BYTES per GPU); the caller supplies every input and output.  Calls on one device
-    share that array, so keep them ordered on one stream.  Returns (out [B, Hq, D], lse2 [B, Hq]).
+    share that array, so keep them ordered on one stream.  Outputs are laid out as pa_v2_decode's with
+    no row maps: request r (member m of a stacked plan) at row r * out_row_step (m * out_row_step).
+    Returns (out [rows, heads, D], lse2 [rows, heads]), rows = batch * stack_members.
     """
     s = plan.struct
     dev = q.device
     ri, ti, oi = plan.device_arrays(dev)
+    rows = s.batch * s.stack_members        # requests, or members of a stacked (cascade level 0) plan
+    heads = s.num_qo_heads // s.stack_members
     if out is None:
-        out = torch.empty(max(s.batch, 1), s.num_qo_heads, s.head_dim, device=dev, dtype=torch.float32)
+        out = torch.empty(max(rows, 1) * s.out_row_step, heads, s.head_dim, device=dev,
+                          dtype=torch.float32)[::s.out_row_step]
     if lse2_out is None:
-        lse2_out = torch.empty(max(s.batch, 1), s.num_qo_heads, device=dev, dtype=torch.float32)
+        lse2_out = torch.empty(max(rows, 1) * s.out_row_step, heads, device=dev, dtype=torch.float32)[::s.out_row_step]
+    if out.shape[0] < rows or tuple(out.shape[1:]) != (heads, s.head_dim):
+        raise ValueError(f"out must hold [{rows}, {heads}, {s.head_dim}]")
+    if lse2_out.shape[0] < rows or tuple(lse2_out.shape[1:]) != (heads,):
+        raise ValueError(f"lse2_out must hold [{rows}, {heads}]")
     if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
         raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
     rc = lib().pa_v2_decode_noalloc(
@@ -411,11 +420,11 @@ def pa_v2_decode_noalloc(plan: Plan, q, k_pool, v_pool, indices, indptr, last_pa
         _dev_ptr(indptr, "indptr", torch.int32), _dev_ptr(last_page_len, "last_page_len", torch.int32),
         _dev_ptr(first_page_offset, "first_page_offset", torch.int32),
         _dev_ptr(ri, "request_indices", torch.int32), _dev_ptr(ti, "kv_tile_indices", torch.int32),
-        _dev_ptr(oi, "o_indptr", torch.int32), float(sm_scale), _dev_ptr(out, "out", torch.float32),
-        _dev_ptr(lse2_out, "lse2_out", torch.float32), _dev_ptr(status, "status", torch.int32), _stream(stream))
+        _dev_ptr(oi, "o_indptr", torch.int32), float(sm_scale), _out_ptr(out, "out", s, heads * s.head_dim),
+        _out_ptr(lse2_out, "lse2_out", s, heads), _dev_ptr(status, "status", torch.int32), _stream(stream))
     if rc != PA_OK:
         raise PaError(rc, "pa_v2_decode_noalloc")
-    return out[:s.batch], lse2_out[:s.batch]
+    return out[:rows], lse2_out[:rows]
 
 
 def decode(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset, sm_scale: float,
