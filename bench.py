@@ -835,17 +835,15 @@ def measure_workload(args):
         Hkv, G = b.num_kv_heads, Hq // b.num_kv_heads
         npre = len(cb.prefix_indices)
         fp1 = torch.zeros(M, dtype=torch.int32)
-        t0 = pa.pa_v2_default_target_ctas(M * Hq, Hkv, D, b.page_size, dt)
-        t1 = pa.pa_v2_default_target_ctas(Hq, Hkv, D, b.page_size, dt)
         cplan = C.cascade_plan(npre, cb.suffix_indptr, cb.suffix_last_page_len, fp1, b.page_size, Hq, Hkv, D, dt,
-                               t0, t1, cb.suffix_lens)
+                               0, cb.suffix_lens)
         c_args = (d.q, d.k_pool, d.v_pool, cb.prefix_indices.to(dev), cb.suffix_indices.to(dev),
                   cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev), fp1.to(dev), b.scale)
         c_out = torch.empty(M, Hq, D, device=dev)
         c_lse = torch.empty(M, Hq, device=dev)
 
         def cascade_step():
-            # level 0 (stacked heads, read in place) + level 1 + one merge: three launches
+            # level 0 (stacked heads, read in place) and level 1 in one launch, then one merge
             C.cascade_decode(cplan, *c_args, out=c_out, lse2_out=c_lse, stream=stream)
 
         cas_bytes = (npre * b.page_size + sum(cb.suffix_lens)) * Hkv * D * 2 * b.k_pool.element_size()

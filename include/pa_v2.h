@@ -280,6 +280,87 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
                               int32_t* member_rows, int32_t* l0_out_rows, int32_t* l1_out_rows,
                               int32_t* merge_indptr);
 
+/* Plans of the two cascade levels (cascade-attention.md, composition and
+ * head-stacking paragraphs) for ONE launch of both (pa_v2_cascade_decode),
+ * and the layout of the merge input they share.
+ *  - Level 0: the `shared_pages` full pages shared by `members` requests, as
+ *    one request whose members' query heads are stacked (stack_members =
+ *    members, num_qo_heads = members * num_qo_heads).
+ *  - Level 1: every request's own table (l1_indptr, l1_last_page_len,
+ *    l1_first_page_offset, l1_seq_lens or null; l1_batch requests, host
+ *    arrays as for pa_v2_plan).  member_requests[m] (host, or null for m) is
+ *    member m's request in that table.
+ * Both levels take ONE chunk size, the smallest whose CTAs -- one chunk's
+ * CTAs (num_kv_heads x q-groups of the level) per chunk, summed over both
+ * levels -- fit `wave_ctas`, so every CTA of the launch reads at most as many
+ * pages as any other (the longest request's size when none fits).  Each plan
+ * is written as pa_v2_plan writes it (arrays into the l0_ / l1_ buffers;
+ * level 0 has one request, so l0_o_indptr holds 2 entries), plan0 with
+ * stack_members = members.  The merge input puts request r's rows together:
+ * its level-0 chunks (members only), then its level-1 chunks.
+ *   merge_indptr [l1_batch + 1] (host): request r's first row; the total,
+ *     merge_indptr[l1_batch], is the rows of merge_v / merge_lse;
+ *   l0_part_rows [members], l1_part_rows [l1_batch] (host): chunk c of
+ *     member m (level 0) / of request r (level 1, c its index among level 1's
+ *     chunks) goes to row part_rows[m or r] + c.
+ * Errors: PA_EINVAL (null pointers, members < 1 or > l1_batch, shared_pages
+ * < 1, wave_ctas < 1, a member_requests entry outside [0, l1_batch) or
+ * repeated), PA_EGEOMETRY, the errors of pa_v2_plan (PA_ECAPACITY with the
+ * plan's num_chunks filled in when a level's arrays are too small). */
+pa_status pa_v2_cascade_plan(int32_t members, int32_t shared_pages, const int32_t* l1_indptr,
+                             const int32_t* l1_last_page_len, const int32_t* l1_first_page_offset,
+                             const int32_t* l1_seq_lens, int32_t l1_batch, const int32_t* member_requests,
+                             int32_t page_size, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t kv_dtype, int32_t wave_ctas, int32_t* l0_request_indices,
+                             int32_t* l0_kv_tile_indices, int32_t l0_cap_chunks, int32_t* l0_o_indptr,
+                             int32_t* l1_request_indices, int32_t* l1_kv_tile_indices, int32_t l1_cap_chunks,
+                             int32_t* l1_o_indptr, int32_t* l0_part_rows, int32_t* l1_part_rows,
+                             int32_t* merge_indptr, pa_v2_plan_t* plan0, pa_v2_plan_t* plan1);
+
+/* One cascade level's device arrays for pa_v2_cascade_decode: its page table
+ * and plan arrays, member_rows (level 0 of a stacked plan: the q row group of
+ * member m, or null for m) and part_rows: the merge-input row of the level's
+ * first chunk of each request (member, for level 0), so that chunk c of
+ * request r lands in row part_rows[r] + c (pa_v2_cascade_plan computes both
+ * levels' part_rows).  DEVICE pointers, owned by the caller. */
+typedef struct pa_v2_cascade_level_t {
+    const int32_t* indices;
+    int64_t num_indices;
+    const int32_t* indptr;
+    const int32_t* last_page_len;
+    const int32_t* first_page_offset;
+    const int32_t* request_indices;
+    const int32_t* kv_tile_indices;
+    const int32_t* member_rows;
+    const int32_t* part_rows;
+} pa_v2_cascade_level_t;
+
+/* Cascade decode in two launches (cascade-attention.md, composition
+ * paragraphs: each request's softmax states over the shared span and over its
+ * own pages merge with the closed form of the split-KV merge, which is
+ * associative).  ONE launch of the tensor-core partial kernel runs both
+ * levels' chunks -- CTAs [0, plan0->num_chunks) level 0, the rest level 1 --
+ * and writes every chunk's normalized partial and lse2 into row
+ * part_rows[r] + c of merge_v [merge_rows, num_qo_heads, D] / merge_lse
+ * [merge_rows, num_qo_heads] (level 0 in member head layout); then
+ * pa_merge_states folds rows merge_indptr[r] .. merge_indptr[r + 1] - 1 into
+ * out [batch_out, num_qo_heads, D] / lse2_out [batch_out, num_qo_heads].
+ * With pa_v2_cascade_plan's part_rows and merge_indptr, request r's rows are
+ * its level-0 chunks (members only) followed by its level-1 chunks.  The two
+ * plans must share kv_dtype, head_dim, page_size and num_kv_heads, level 0's
+ * query heads must be level 1's times its stack_members, and both must take
+ * the tensor-core kernel with the same staging (else PA_EUNSUPPORTED); a
+ * level without chunks is PA_EINVAL.  q, the
+ * pools and num_pages are shared; level 0 reads q through its stacked plan.
+ * DEVICE pointers; stream ordered; errors as pa_v2_decode_partial and
+ * pa_merge_states. */
+pa_status pa_v2_cascade_decode(const pa_v2_plan_t* plan0, const pa_v2_plan_t* plan1,
+                               const pa_v2_cascade_level_t* level0, const pa_v2_cascade_level_t* level1,
+                               const float* q, const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                               int64_t num_pages, float sm_scale, float* merge_v, float* merge_lse,
+                               int32_t merge_rows, const int32_t* merge_indptr, int32_t batch_out, float* out,
+                               float* lse2_out, int32_t* status, void* cuda_stream);
+
 /* Partial attention with a second K stream (sparse-paged-decode.md, issue
  * #904: the DSA paragraphs, third way out -- "a row stride plus a second K
  * stream").  The score of visible token t (resolved through the page table

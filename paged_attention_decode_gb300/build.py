@@ -20,8 +20,8 @@ LIB_NAME = "libpa_v2.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["pa_plan.cpp", "pa_cascade.cpp", "pa_partial.cu", "pa_partial_simt.cu", "pa_partial_tc.cu", "pa_merge.cu",
-           "pa_noalloc.cu", "pa_select.cu", "pa_host_step.cpp", "pa_partial_extra.cu",
+SOURCES = ["pa_plan.cpp", "pa_cascade.cpp", "pa_partial.cu", "pa_partial_simt.cu", "pa_partial_tc.cu",
+           "pa_partial_tc_cascade.cu", "pa_merge.cu", "pa_noalloc.cu", "pa_select.cu", "pa_host_step.cpp", "pa_partial_extra.cu",
            "pa_partial_extra_tc.cu", "pa_partial_extra_tc05.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

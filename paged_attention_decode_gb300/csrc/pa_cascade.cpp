@@ -118,3 +118,92 @@ extern "C" pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* i
   }
   return PA_OK;
 }
+
+
+// The two cascade levels planned for one launch (cascade-attention.md): one chunk size for both levels,
+// the smallest whose CTAs fit the wave, so that no CTA of the launch reads more pages than another; and the
+// merge input laid out request by request (level-0 chunks of a member, then its level-1 chunks), so that one
+// merge folds every request's states.
+extern "C" pa_status pa_v2_cascade_plan(int32_t members, int32_t shared_pages, const int32_t* l1_indptr,
+                                        const int32_t* l1_last_page_len, const int32_t* l1_first_page_offset,
+                                        const int32_t* l1_seq_lens, int32_t l1_batch, const int32_t* member_requests,
+                                        int32_t page_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t kv_dtype, int32_t wave_ctas,
+                                        int32_t* l0_request_indices, int32_t* l0_kv_tile_indices,
+                                        int32_t l0_cap_chunks, int32_t* l0_o_indptr, int32_t* l1_request_indices,
+                                        int32_t* l1_kv_tile_indices, int32_t l1_cap_chunks, int32_t* l1_o_indptr,
+                                        int32_t* l0_part_rows, int32_t* l1_part_rows, int32_t* merge_indptr,
+                                        pa_v2_plan_t* plan0, pa_v2_plan_t* plan1) {
+  if (!l1_indptr || !plan0 || !plan1 || !l0_o_indptr || !l1_o_indptr || !l0_part_rows || !merge_indptr ||
+      (l1_batch > 0 && !l1_part_rows) || members < 1 || members > l1_batch || shared_pages < 1 ||
+      wave_ctas < 1 || num_kv_heads < 1 || num_qo_heads < num_kv_heads || num_qo_heads % num_kv_heads != 0 ||
+      num_qo_heads > INT32_MAX / members)
+    return PA_EINVAL;
+  if (l1_indptr[0] != 0) return PA_EGEOMETRY;
+  // member m's request in the level-1 table: distinct, in range
+  std::vector<int32_t> member_of(l1_batch, -1), req_of(members);
+  for (int32_t m = 0; m < members; ++m) {
+    const int32_t r = member_requests ? member_requests[m] : m;
+    if (r < 0 || r >= l1_batch || member_of[r] >= 0) return PA_EINVAL;
+    member_of[r] = m;
+    req_of[m] = r;
+  }
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const int32_t hpc0 = pa_v2_q_heads_per_cta(members * group, head_dim, kv_dtype);
+  const int32_t hpc1 = pa_v2_q_heads_per_cta(group, head_dim, kv_dtype);
+  if (hpc0 == 0 || hpc1 == 0) return PA_EUNSUPPORTED;
+  const int64_t per0 = static_cast<int64_t>(num_kv_heads) * ((members * group + hpc0 - 1) / hpc0);
+  const int64_t per1 = static_cast<int64_t>(num_kv_heads) * ((group + hpc1 - 1) / hpc1);
+  std::vector<int64_t> pages1(l1_batch);
+  int64_t longest = shared_pages;
+  for (int32_t r = 0; r < l1_batch; ++r) {
+    pages1[r] = static_cast<int64_t>(l1_indptr[r + 1]) - l1_indptr[r];
+    if (pages1[r] < 0) return PA_EGEOMETRY;
+    longest = std::max(longest, pages1[r]);
+  }
+  // one chunk size for both levels: the smallest whose CTAs (non-increasing in the size) fit the wave
+  auto ctas = [&](int64_t size) {
+    int64_t n = per0 * ((shared_pages + size - 1) / size);
+    for (int64_t p : pages1) n += per1 * (p > size ? (p + size - 1) / size : 1);
+    return n;
+  };
+  int64_t lo = 1, hi = longest;
+  if (ctas(hi) > wave_ctas) {
+    lo = hi;
+  } else {
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (ctas(mid) <= wave_ctas) hi = mid; else lo = mid + 1;
+    }
+  }
+  const int32_t ppc = static_cast<int32_t>(lo);
+
+  const int32_t ip0[2] = {0, shared_pages};
+  const int32_t lp0[1] = {page_size};
+  const int32_t fp0[1] = {0};
+  pa_status rc = pa_v2_plan(ip0, lp0, fp0, nullptr, 1, page_size, members * num_qo_heads, num_kv_heads, head_dim,
+                            kv_dtype, wave_ctas, ppc, l0_request_indices, l0_kv_tile_indices, l0_cap_chunks,
+                            l0_o_indptr, plan0);
+  if (rc != PA_OK) return rc;
+  plan0->stack_members = members;
+  rc = pa_v2_plan(l1_indptr, l1_last_page_len, l1_first_page_offset, l1_seq_lens, l1_batch, page_size,
+                  num_qo_heads, num_kv_heads, head_dim, kv_dtype, wave_ctas, ppc, l1_request_indices,
+                  l1_kv_tile_indices, l1_cap_chunks, l1_o_indptr, plan1);
+  if (rc != PA_OK) return rc;
+
+  // merge input: request r's rows are its level-0 chunks (members), then its level-1 chunks
+  const int32_t n0 = plan0->num_chunks;
+  int32_t row = 0;
+  for (int32_t r = 0; r < l1_batch; ++r) {
+    merge_indptr[r] = row;
+    const int32_t first1 = l1_o_indptr[r];
+    if (member_of[r] >= 0) {
+      l0_part_rows[member_of[r]] = row;
+      row += n0;
+    }
+    l1_part_rows[r] = row - first1;  // chunk j of request r (o_indptr[r] <= j) lands at row + j - first1
+    row += l1_o_indptr[r + 1] - first1;
+  }
+  merge_indptr[l1_batch] = row;
+  return PA_OK;
+}

@@ -32,7 +32,7 @@ struct PartialParams {
   // fused decode (pa_v2_decode): the last CTA of a (request, kv head, q-group)
   // merges that request's chunks into out / lse_final
   const int32_t* o_indptr;
-  int32_t* counters;   // [batch * gridDim.y], zero between launches
+  int32_t* counters;   // [batch * (CTA rows per chunk)], zero between launches
   float* out;          // [batch, Hq, D]
   float* lse_final;    // [batch, Hq]
   int32_t fused;
@@ -44,6 +44,10 @@ struct PartialParams {
   int32_t out_row_step;    // final output row r is written at row r * out_row_step
   const int32_t* member_rows;  // stacked plans: request (q row group) of member m, or null for m
   const int32_t* out_rows;     // final output row of request r (member m when stacked), or null
+  // partial rows (not fused): chunk c of request r (member m when stacked) goes to workspace row
+  // part_rows[r] + c instead of row c, heads in member layout when stacked (one merge input holding
+  // both cascade levels' chunks of each request, contiguously)
+  const int32_t* part_rows;
   int64_t num_pages;
   int64_t num_indices;
   int32_t single_pages;  // > 0: a one-request plan of this many pages (chunk c is tile c of request 0)
@@ -102,6 +106,19 @@ __device__ __forceinline__ size_t out_row(const PartialParams& p, int r, int h) 
   }
   const size_t row = p.out_rows ? (size_t)p.out_rows[r] : (size_t)r * p.out_row_step;
   return row * p.num_qo_heads + h;
+}
+
+// Workspace row (in units of head_dim) of chunk c's partial for query head h when the launch maps
+// partial rows (p.part_rows): row part_rows[r] + c, or, stacked, part_rows[m] + c at member head hm.
+// r: the chunk's request as validated by chunk_geom.
+__device__ __forceinline__ size_t part_row(const PartialParams& p, int c, int r, int h) {
+  if (p.stack_members > 1) {
+    const int within = h % p.group;
+    const int m = within / p.member_group;
+    const int hm = (h / p.group) * p.member_group + within % p.member_group;
+    return ((size_t)p.part_rows[m] + c) * p.member_heads + hm;
+  }
+  return ((size_t)p.part_rows[r] + c) * p.num_qo_heads + h;
 }
 
 struct ChunkGeom {
@@ -193,10 +210,11 @@ __device__ __forceinline__ StageGeom stage_geom(const ChunkGeom& g, int j, int p
 // when final_output, to the final output of request `row`.  ms/ls:
 // [NW][HP]; accs: [NW][HP][D] (unnormalized, relative to each warp's max).
 // Called by all threads after a __syncthreads() that follows the state writes.
-template <int HP, int D, int NW>
+// MAPPED: partial rows follow p.part_rows (the cascade launch); other launches compile without it.
+template <int HP, int D, int NW, bool MAPPED = false>
 __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, const float* ms, const float* ls,
                                                         const float* accs, int row, int h_first, int nheads,
-                                                        bool final_output) {
+                                                        bool final_output, int req = 0) {
   for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
     const int h = idx / D;
     const int d = idx % D;
@@ -219,6 +237,10 @@ __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, 
       const size_t o = out_row(p, row, h_first + h);
       p.out[o * D + d] = out;
       if (d == 0) p.lse_final[o] = lse;
+    } else if (MAPPED) {
+      const size_t o = part_row(p, row, req, h_first + h);
+      p.v_out[o * D + d] = out;
+      if (d == 0) p.lse_out[o] = lse;
     } else {
       const size_t o = (size_t)row * p.num_qo_heads + h_first + h;
       p.v_out[o * D + d] = out;
@@ -244,7 +266,7 @@ __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, 
 // scratch: >= 6 * NW * 32 floats of shared memory no longer in use.
 template <int D, int NW>
 __device__ __forceinline__ void fused_merge(const PartialParams& p, float* scratch, int r, int h_first,
-                                            int nheads, int num_chunks) {
+                                            int nheads, int num_chunks, int y, int ny) {
   __shared__ int s_last;
   constexpr int NT = NW * 32;
   constexpr int Q = D / 4;   // float4 slices per head row
@@ -257,7 +279,7 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, float* scrat
   }
   __syncthreads();  // every thread's partial stores precede the release below
   if (threadIdx.x == 0) {
-    int* ctr = p.counters + (size_t)r * gridDim.y + blockIdx.y;
+    int* ctr = p.counters + (size_t)r * ny + y;
     int prev;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
     const int last = prev == (n1 - n0) - 1;
@@ -361,19 +383,24 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, float* scrat
 // decode) merge the request when this CTA is the last of its group.  A request
 // with a single chunk writes straight to the final output.  scratch: the CTA's
 // shared memory that is free once the states have been combined.
-template <int HP, int D, int NW>
+// num_chunks, y, ny: the launch's chunk count, this CTA's row among the CTAs of a chunk and their number
+// (-1: the grid's own, gridDim.x, blockIdx.y, gridDim.y; a launch that runs two plans passes its plan's).
+template <int HP, int D, int NW, bool MAPPED = false>
 __device__ __forceinline__ void finish_chunk(const PartialParams& p, const ChunkGeom& g, const float* ms,
                                              const float* ls, const float* accs, float* scratch, int c, int r,
-                                             int h_first, int nheads) {
+                                             int h_first, int nheads, int num_chunks = -1, int y = -1,
+                                             int ny = -1) {
+  if (MAPPED && g.bad) return;  // no row of a mapped workspace belongs to a chunk with a bad request
   bool direct = false;
   if (p.fused && !g.bad) {
     const int n0 = p.o_indptr[r], n1 = p.o_indptr[r + 1];
     direct = n1 - n0 == 1;
   }
-  combine_warps_and_store<HP, D, NW>(p, ms, ls, accs, direct ? r : c, h_first, nheads, direct);
+  combine_warps_and_store<HP, D, NW, MAPPED>(p, ms, ls, accs, direct ? r : c, h_first, nheads, direct, r);
   if (p.fused && !g.bad && !direct) {
     __syncthreads();  // scratch aliases the state arrays just read
-    fused_merge<D, NW>(p, scratch, r, h_first, nheads, gridDim.x);
+    fused_merge<D, NW>(p, scratch, r, h_first, nheads, num_chunks < 0 ? (int)gridDim.x : num_chunks,
+                       y < 0 ? (int)blockIdx.y : y, ny < 0 ? (int)gridDim.y : ny);
   }
 }
 
@@ -396,6 +423,9 @@ int occupancy_partial_simt(int kv_dtype, int head_dim, int hpc, int* blocks_per_
 // Tensor-core kernel (f16 / bf16 pools).  use_tma: stage with TMA (page sizes
 // whose pages start on 8-row boundaries of a stage) instead of cp.async.
 int launch_partial_tc(const LaunchArgs& a, bool use_tma);
+// Two plans over the same pools in one launch: a's plan on CTA columns [0, a.num_chunks), p1's n1 chunks
+// after them (the cascade levels); both plans fused (each CTA group merges its own requests).
+int launch_partial_tc_two_plans(const LaunchArgs& a, const PartialParams& p1, int n1, bool use_tma);
 int occupancy_partial_tc(int kv_dtype, int head_dim, int hpc, bool use_tma, int* blocks_per_sm);
 
 // Second-K-stream kernels (head_dim 512 + extra 64; f16 / bf16 pools): CUDA

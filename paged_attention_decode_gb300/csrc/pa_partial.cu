@@ -134,12 +134,17 @@ struct FusedArgs {
   const int32_t* out_rows;
 };
 
-pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
-                        int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
-                        const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
-                        const int32_t* request_indices, const int32_t* kv_tile_indices, float sm_scale,
-                        float* v_out, float* lse2_out, int32_t* status, void* cuda_stream, const FusedArgs* fused) {
+// Validate a decode launch and fill its launch arguments (tensor maps in *tm_k / *tm_v, which must outlive
+// the launch); *tc / *tma say which kernel and staging it takes.  A plan with no chunks returns PA_OK with
+// a->num_chunks = 0 and nothing to launch.
+pa_status prepare_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
+                         int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
+                         const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
+                         const int32_t* request_indices, const int32_t* kv_tile_indices, float sm_scale,
+                         float* v_out, float* lse2_out, int32_t* status, void* cuda_stream, const FusedArgs* fused,
+                         pa::LaunchArgs* args, CUtensorMap* tm_k, CUtensorMap* tm_v, bool* tc_out, bool* tma_out) {
   if (!plan) return PA_EINVAL;
+  args->num_chunks = 0;
   if (plan->num_chunks == 0) return PA_OK;
   if (!q || !k_pool || !v_pool || !indices || !indptr || !last_page_len || !first_page_offset ||
       !request_indices || !kv_tile_indices || !v_out || !lse2_out)
@@ -164,19 +169,18 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
   if (!tc && hpc > 8) return PA_EUNSUPPORTED;
   const bool tma = !tc || pa::tc_uses_tma(ps);
 
-  alignas(64) CUtensorMap tm_k, tm_v;
-  std::memset(&tm_k, 0, sizeof(tm_k));
-  std::memset(&tm_v, 0, sizeof(tm_v));
+  std::memset(tm_k, 0, sizeof(*tm_k));
+  std::memset(tm_v, 0, sizeof(*tm_v));
   if (tma) {
     const int box_rows = ps <= pa::kStageRows ? ps : pa::kStageRows;
     const int box_d = tc ? 64 : D;
     const CUtensorMapSwizzle sw = tc ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    if (!pa::make_pool_map(&tm_k, k_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw) ||
-        !pa::make_pool_map(&tm_v, v_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw))
+    if (!pa::make_pool_map(tm_k, k_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw) ||
+        !pa::make_pool_map(tm_v, v_pool, kv_dtype, num_pages * ps, plan->num_kv_heads, D, box_d, box_rows, sw))
       return PA_ECUDA;
   }
 
-  pa::LaunchArgs a;
+  pa::LaunchArgs& a = *args;
   pa::PartialParams& p = a.p;
   std::memset(&p, 0, sizeof(p));
   p.q = q;
@@ -221,12 +225,29 @@ pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_
   p.member_heads = plan->num_qo_heads / M;
   p.member_group = p.group / M;
   p.out_row_step = plan->out_row_step;
-  a.tm_k = &tm_k;
-  a.tm_v = &tm_v;
+  a.tm_k = tm_k;
+  a.tm_v = tm_v;
   a.kv_dtype = kv_dtype;
   a.head_dim = D;
   a.num_chunks = plan->num_chunks;
   a.stream = static_cast<cudaStream_t>(cuda_stream);
+  *tc_out = tc;
+  *tma_out = tma;
+  return PA_OK;
+}
+
+pa_status launch_decode(const pa_v2_plan_t* plan, const float* q, const void* k_pool, const void* v_pool,
+                        int32_t kv_dtype, int64_t num_pages, const int32_t* indices, int64_t num_indices,
+                        const int32_t* indptr, const int32_t* last_page_len, const int32_t* first_page_offset,
+                        const int32_t* request_indices, const int32_t* kv_tile_indices, float sm_scale,
+                        float* v_out, float* lse2_out, int32_t* status, void* cuda_stream, const FusedArgs* fused) {
+  alignas(64) CUtensorMap tm_k, tm_v;
+  pa::LaunchArgs a;
+  bool tc = false, tma = false;
+  const pa_status rc = prepare_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr,
+                                      last_page_len, first_page_offset, request_indices, kv_tile_indices, sm_scale,
+                                      v_out, lse2_out, status, cuda_stream, fused, &a, &tm_k, &tm_v, &tc, &tma);
+  if (rc != PA_OK || a.num_chunks == 0) return rc;
   return (pa_status)(tc ? pa::launch_partial_tc(a, tma) : pa::launch_partial_simt(a));
 }
 
@@ -256,4 +277,43 @@ extern "C" pa_status pa_v2_decode(const pa_v2_plan_t* plan, const float* q, cons
   return launch_decode(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, num_indices, indptr, last_page_len,
                        first_page_offset, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse,
                        status, cuda_stream, &f);
+}
+
+// Both cascade levels in one launch of the tensor-core kernel, writing every chunk's partial into the rows
+// of one merge input, then the merge of each request's rows (cascade-attention.md, composition paragraphs).
+extern "C" pa_status pa_v2_cascade_decode(const pa_v2_plan_t* plan0, const pa_v2_plan_t* plan1,
+                                          const pa_v2_cascade_level_t* level0, const pa_v2_cascade_level_t* level1,
+                                          const float* q, const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                                          int64_t num_pages, float sm_scale, float* merge_v, float* merge_lse,
+                                          int32_t merge_rows, const int32_t* merge_indptr, int32_t batch_out,
+                                          float* out, float* lse2_out, int32_t* status, void* cuda_stream) {
+  if (!plan0 || !plan1 || !level0 || !level1 || !merge_v || !merge_lse || !merge_indptr || !out || !lse2_out ||
+      merge_rows < 0 || batch_out < 0 || !level0->part_rows || (plan1->num_chunks > 0 && !level1->part_rows))
+    return PA_EINVAL;
+  if (plan0->stack_members < 1 || plan0->kv_dtype != plan1->kv_dtype || plan0->head_dim != plan1->head_dim ||
+      plan0->page_size != plan1->page_size || plan0->num_kv_heads != plan1->num_kv_heads ||
+      plan0->num_qo_heads != plan1->num_qo_heads * plan0->stack_members || plan1->stack_members != 1)
+    return PA_EUNSUPPORTED;
+  const pa_v2_cascade_level_t* lv[2] = {level0, level1};
+  const pa_v2_plan_t* pl[2] = {plan0, plan1};
+  alignas(64) CUtensorMap tk[2], tv[2];
+  pa::LaunchArgs a[2];
+  bool tc[2] = {false, false}, tma[2] = {false, false};
+  for (int l = 0; l < 2; ++l) {
+    const pa_status rc =
+        prepare_decode(pl[l], q, k_pool, v_pool, kv_dtype, num_pages, lv[l]->indices, lv[l]->num_indices,
+                       lv[l]->indptr, lv[l]->last_page_len, lv[l]->first_page_offset, lv[l]->request_indices,
+                       lv[l]->kv_tile_indices, sm_scale, merge_v, merge_lse, status, cuda_stream, nullptr, &a[l],
+                       &tk[l], &tv[l], &tc[l], &tma[l]);
+    if (rc != PA_OK) return rc;
+    a[l].p.part_rows = lv[l]->part_rows;
+    a[l].p.member_rows = lv[l]->member_rows;
+  }
+  if (a[0].num_chunks == 0 || a[1].num_chunks == 0) return PA_EINVAL;  // each level has at least one chunk
+  if (!tc[0] || !tc[1] || tma[0] != tma[1]) return PA_EUNSUPPORTED;
+  // one launch: the tensor maps depend only on the shared pools, dtype, page size and head counts
+  const int rc = pa::launch_partial_tc_two_plans(a[0], a[1].p, a[1].num_chunks, tma[0]);
+  if (rc != PA_OK) return (pa_status)rc;
+  return pa_merge_states(merge_v, merge_lse, merge_indptr, batch_out, merge_rows, plan1->num_qo_heads,
+                         plan1->head_dim, out, lse2_out, status, cuda_stream);
 }

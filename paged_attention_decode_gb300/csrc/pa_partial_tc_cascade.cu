@@ -1,0 +1,80 @@
+// pa_partial_tc_cascade.cu -- the two cascade levels in one launch of the
+// tensor-core partial kernel (cascade-attention.md, issue #903, composition and
+// head-stacking paragraphs): CTA columns [0, split) run level 0's chunks (the
+// members' heads stacked over the shared pages), the rest level 1's.  Kept in
+// its own translation unit so that the one-plan kernel's module is unchanged.
+#include "pa_partial_tc_body.cuh"
+
+namespace pa {
+namespace {
+
+// Two plans over the same pools in one launch (the two cascade levels, cascade-attention.md): CTA columns
+// [0, split) run plan p0's chunks, the rest plan p1's (n1 chunks); a CTA whose row is past its plan's CTAs
+// per chunk leaves before touching memory.  Each plan writes its partials (and merges, when fused) as its own launch would.
+template <typename T, int D, int NT, int NSW, int NW, bool USE_TMA>
+__global__ void __launch_bounds__(NW * 32)
+    pa_v2_partial_tc_two_plan_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PartialParams p0,
+                                     const __grid_constant__ PartialParams p1, const int split, const int n1) {
+  if ((int)blockIdx.x < split) {
+    const int ny = p0.num_kv_heads * p0.q_groups;
+    if ((int)blockIdx.y < ny) partial_tc_body<T, D, NT, NSW, NW, USE_TMA, true>(tm_k, tm_v, p0, blockIdx.x, blockIdx.y, split, ny);
+  } else {
+    const int ny = p1.num_kv_heads * p1.q_groups;
+    if ((int)blockIdx.y < ny)
+      partial_tc_body<T, D, NT, NSW, NW, USE_TMA, true>(tm_k, tm_v, p1, blockIdx.x - split, blockIdx.y, n1, ny);
+  }
+}
+
+using TcKernel2 = void (*)(const CUtensorMap, const CUtensorMap, const PartialParams, const PartialParams, const int,
+                           const int);
+
+struct Tc2Instance {
+  TcKernel2 fn;
+  size_t smem;
+};
+
+template <typename T, int D, int NT, bool TMA>
+Tc2Instance tc2_make() {
+  return {pa_v2_partial_tc_two_plan_kernel<T, D, NT, kTcRing, kTcWarps, TMA>,
+          (size_t)TcLayout<D, NT, kTcRing, kTcWarps>::ALLOC};
+}
+
+template <typename T, int D, bool TMA>
+bool tc2_pick_nt(int hpc, Tc2Instance* out) {
+  if (hpc <= 8) { *out = tc2_make<T, D, 1, TMA>(); return true; }
+  if (hpc <= 16) { *out = tc2_make<T, D, 2, TMA>(); return true; }
+  return false;
+}
+
+template <typename T, int D>
+bool tc2_pick_stage(int hpc, bool tma, Tc2Instance* out) {
+  return tma ? tc2_pick_nt<T, D, true>(hpc, out) : tc2_pick_nt<T, D, false>(hpc, out);
+}
+
+bool tc2_pick(int dtype, int D, int hpc, bool tma, Tc2Instance* out) {
+  if (dtype == PA_F16) {
+    if (D == 64) return tc2_pick_stage<__half, 64>(hpc, tma, out);
+    if (D == 128) return tc2_pick_stage<__half, 128>(hpc, tma, out);
+  } else if (dtype == PA_BF16) {
+    if (D == 64) return tc2_pick_stage<__nv_bfloat16, 64>(hpc, tma, out);
+    if (D == 128) return tc2_pick_stage<__nv_bfloat16, 128>(hpc, tma, out);
+  }
+  return false;
+}
+
+}  // namespace
+
+int launch_partial_tc_two_plans(const LaunchArgs& a, const PartialParams& p1, int n1, bool use_tma) {
+  Tc2Instance inst;
+  const int hpc = a.p.hpc > p1.hpc ? a.p.hpc : p1.hpc;  // one instance serves both plans' head groups
+  if (!tc2_pick(a.kv_dtype, a.head_dim, hpc, use_tma, &inst)) return PA_EUNSUPPORTED;
+  if (!prepare_kernel(reinterpret_cast<const void*>(inst.fn), inst.smem)) return PA_ECUDA;
+  const int y0 = a.p.num_kv_heads * a.p.q_groups, y1 = p1.num_kv_heads * p1.q_groups;
+  dim3 grid(a.num_chunks + n1, y0 > y1 ? y0 : y1);
+  const cudaError_t rc = launch_dependent(inst.fn, grid, dim3(kTcWarps * 32), inst.smem, a.stream, *a.tm_k, *a.tm_v,
+                                          a.p, p1, a.num_chunks, n1);
+  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+}  // namespace pa

@@ -35,8 +35,18 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
                "pa_v2_decode_partial_extra", "pa_v2_selftest_wait", "pa_v2_host_graph_create",
                "pa_v2_host_graph_run", "pa_v2_host_graph_destroy", "pa_v2_wave_fit_pages_per_chunk",
-               "pa_v2_balanced_pages_per_chunk", "pa_status_from_device", "pa_status_string", "pa_version")
+               "pa_v2_balanced_pages_per_chunk", "pa_v2_cascade_plan", "pa_v2_cascade_decode",
+               "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+class CascadeLevelStruct(ctypes.Structure):
+    """Mirror of pa_v2_cascade_level_t (device pointers of one cascade level)."""
+
+    _fields_ = [("indices", ctypes.c_void_p), ("num_indices", ctypes.c_int64), ("indptr", ctypes.c_void_p),
+                ("last_page_len", ctypes.c_void_p), ("first_page_offset", ctypes.c_void_p),
+                ("request_indices", ctypes.c_void_p), ("kv_tile_indices", ctypes.c_void_p),
+                ("member_rows", ctypes.c_void_p), ("part_rows", ctypes.c_void_p)]
 
 
 class PaError(RuntimeError):
@@ -84,6 +94,12 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_cascade_detect.restype = i32
         L.pa_v2_cascade_split.argtypes = [P, P, P, P, i32, P, i32, P, P, P, P, P, P, P, P]
         L.pa_v2_cascade_split.restype = i32
+        L.pa_v2_cascade_plan.argtypes = [i32, i32, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, P, P, i32, P,
+                                         P, P, i32, P, P, P, P, PP, PP]
+        L.pa_v2_cascade_plan.restype = i32
+        CL = ctypes.POINTER(CascadeLevelStruct)
+        L.pa_v2_cascade_decode.argtypes = [PP, PP, CL, CL, P, P, P, i32, i64, f32, P, P, i32, P, i32, P, P, P, P]
+        L.pa_v2_cascade_decode.restype = i32
         L.pa_v2_decode.restype = i32
         L.pa_v2_decode_noalloc.argtypes = [PP, P, P, P, i32, i64, P, i64, P, P, P, P, P, P, f32, P, P, P, P]
         L.pa_v2_decode_noalloc.restype = i32
@@ -386,6 +402,99 @@ def pa_v2_cascade_split(indptr, indices, last_page_len, first_page_offset, membe
     return {"l1_indptr": l1_ip, "l1_indices": l1_idx[:n1], "l1_last_page_len": l1_lp[:B],
             "l1_first_page_offset": l1_fp[:B], "member_rows": mrows[:M], "l0_out_rows": l0_rows[:M],
             "l1_out_rows": l1_rows[:B], "merge_indptr": m_ip}
+
+
+@dataclass
+class CascadePlans:
+    """Both cascade levels' plans and the merge input they share (pa_v2_cascade_plan); host arrays."""
+
+    level0: Plan
+    level1: Plan
+    l0_part_rows: torch.Tensor   # [members]
+    l1_part_rows: torch.Tensor   # [l1_batch]
+    merge_indptr: torch.Tensor   # [l1_batch + 1]
+
+    @property
+    def merge_rows(self) -> int:
+        return int(self.merge_indptr[-1])
+
+
+def pa_v2_cascade_plan(members: int, shared_pages: int, l1_indptr, l1_last_page_len, l1_first_page_offset,
+                       page_size: int, num_qo_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int,
+                       wave_ctas: int, l1_seq_lens=None, member_requests=None) -> CascadePlans:
+    """Plans of both cascade levels for one launch, and the merge layout (pa_v2_cascade_plan); host arrays."""
+    ip, lp, fp = _host_i32(l1_indptr), _host_i32(l1_last_page_len), _host_i32(l1_first_page_offset)
+    B = lp.numel()
+    sl = _host_i32(l1_seq_lens) if l1_seq_lens is not None else None
+    mr = _host_i32(member_requests) if member_requests is not None else None
+    cap1 = int((ip[1:] - ip[:-1]).clamp(min=1).sum()) if B else 1
+    cap0 = max(1, int(shared_pages))
+    r0, t0, o0 = (torch.zeros(cap0, dtype=torch.int32), torch.zeros(cap0, dtype=torch.int32),
+                  torch.zeros(2, dtype=torch.int32))
+    r1, t1, o1 = (torch.zeros(max(cap1, 1), dtype=torch.int32), torch.zeros(max(cap1, 1), dtype=torch.int32),
+                  torch.zeros(B + 1, dtype=torch.int32))
+    pr0, pr1 = torch.zeros(max(members, 1), dtype=torch.int32), torch.zeros(max(B, 1), dtype=torch.int32)
+    mi = torch.zeros(B + 1, dtype=torch.int32)
+    s0, s1 = PlanStruct(), PlanStruct()
+    rc = lib().pa_v2_cascade_plan(members, shared_pages, ip.data_ptr(), lp.data_ptr() if B else None,
+                                  fp.data_ptr() if B else None, sl.data_ptr() if sl is not None else None, B,
+                                  mr.data_ptr() if mr is not None else None, page_size, num_qo_heads, num_kv_heads,
+                                  head_dim, kv_dtype, wave_ctas, r0.data_ptr(), t0.data_ptr(), cap0, o0.data_ptr(),
+                                  r1.data_ptr(), t1.data_ptr(), max(cap1, 1), o1.data_ptr(), pr0.data_ptr(),
+                                  pr1.data_ptr(), mi.data_ptr(), ctypes.byref(s0), ctypes.byref(s1))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_cascade_plan")
+    return CascadePlans(Plan(s0, r0[:s0.num_chunks].clone(), t0[:s0.num_chunks].clone(), o0),
+                        Plan(s1, r1[:s1.num_chunks].clone(), t1[:s1.num_chunks].clone(), o1),
+                        pr0[:members].clone(), pr1[:B].clone(), mi)
+
+
+def cascade_level(plan: Plan, indices, indptr, last_page_len, first_page_offset, part_rows,
+                  member_rows=None) -> CascadeLevelStruct:
+    """A pa_v2_cascade_level_t for `plan` (device tensors; the plan's chunk arrays are its own device
+    copies, kept alive by the struct)."""
+    dev = indices.device
+    ri, ti, _ = plan.device_arrays(dev)
+    lv = CascadeLevelStruct()
+    lv.indices = _dev_ptr(indices, "indices", torch.int32)
+    lv.num_indices = indices.numel()
+    lv.indptr = _dev_ptr(indptr, "indptr", torch.int32)
+    lv.last_page_len = _dev_ptr(last_page_len, "last_page_len", torch.int32)
+    lv.first_page_offset = _dev_ptr(first_page_offset, "first_page_offset", torch.int32)
+    lv.request_indices = _dev_ptr(ri, "request_indices", torch.int32)
+    lv.kv_tile_indices = _dev_ptr(ti, "kv_tile_indices", torch.int32)
+    lv.member_rows = _dev_ptr(member_rows, "member_rows", torch.int32)
+    lv.part_rows = _dev_ptr(part_rows, "part_rows", torch.int32)
+    lv._keep = (ri, ti, part_rows, member_rows)
+    return lv
+
+
+def pa_v2_cascade_decode(cps: CascadePlans, level0: CascadeLevelStruct, level1: CascadeLevelStruct, q, k_pool,
+                         v_pool, sm_scale: float, merge_v, merge_lse, merge_indptr, out=None, lse2_out=None,
+                         status=None, stream=None):
+    """Both cascade levels in one launch writing one merge input, then the merge (pa_v2_cascade_decode).
+    Returns (out [B, Hq, D], lse2 [B, Hq]), B = the level-1 batch."""
+    p1 = cps.level1.struct
+    H, D, B = p1.num_qo_heads, p1.head_dim, p1.batch
+    dev = q.device
+    if out is None:
+        out = torch.empty(max(B, 1), H, D, device=dev, dtype=torch.float32)
+    if lse2_out is None:
+        lse2_out = torch.empty(max(B, 1), H, device=dev, dtype=torch.float32)
+    if tuple(merge_v.shape) != (cps.merge_rows, H, D) or tuple(merge_lse.shape) != (cps.merge_rows, H):
+        raise ValueError(f"merge_v / merge_lse must be [{cps.merge_rows}, {H}, {D}] / [{cps.merge_rows}, {H}]")
+    if k_pool.dtype not in KV_DTYPES or v_pool.dtype != k_pool.dtype or k_pool.shape != v_pool.shape:
+        raise ValueError("k_pool and v_pool must share one of float32/float16/bfloat16 and a shape")
+    rc = lib().pa_v2_cascade_decode(
+        ctypes.byref(cps.level0.struct), ctypes.byref(p1), ctypes.byref(level0), ctypes.byref(level1),
+        _dev_ptr(q, "q", torch.float32), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+        KV_DTYPES[k_pool.dtype], k_pool.shape[0], float(sm_scale), _dev_ptr(merge_v, "merge_v", torch.float32),
+        _dev_ptr(merge_lse, "merge_lse", torch.float32), cps.merge_rows,
+        _dev_ptr(merge_indptr, "merge_indptr", torch.int32), B, _dev_ptr(out, "out", torch.float32),
+        _dev_ptr(lse2_out, "lse2_out", torch.float32), _dev_ptr(status, "status", torch.int32), _stream(stream))
+    if rc != PA_OK:
+        raise PaError(rc, "pa_v2_cascade_decode")
+    return out[:B], lse2_out[:B]
 
 
 def pa_v2_decode_noalloc(plan: Plan, q, k_pool, v_pool, indices, indptr, last_page_len, first_page_offset,

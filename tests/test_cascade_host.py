@@ -1,6 +1,7 @@
 """Cascade detection and level split on the host (no GPU): the library against the oracle's rule."""
 import random
 
+import pytest
 import torch
 
 import oracle
@@ -113,12 +114,78 @@ def test_split_rebuilds_the_flat_tables():
         assert sp["l0_out_rows"].tolist() == [mi[r] for r in members]
 
 
-def test_split_wave_and_chunk_fit():
+def test_cascade_plan_by_hand():
+    # 4 members share 512 pages; suffixes of 25, 94, 62 and 91 pages; one wave of 152 CTAs, 8 CTAs per chunk at
+    # either level (Hkv 8, one q-group).  One chunk size for both levels: 47 pages make 11 + (1 + 2 + 2 + 2) = 18
+    # chunks = 144 CTAs; 46 pages would make 12 + (1 + 3 + 2 + 2) = 20 = 160
+    c = pa.pa_v2_cascade_plan(4, 512, [0, 25, 119, 181, 272], [16, 4, 7, 16], [0, 0, 0, 0], 16, 32, 8, 128,
+                              pa.PA_F16, 152)
+    assert (c.level0.pages_per_chunk, c.level0.num_chunks, c.level1.num_chunks) == (47, 11, 7)
+    assert c.level1.pages_per_chunk == 47 and c.level0.total_ctas + c.level1.total_ctas == 144
+    assert (c.level0.stack_members, c.level0.num_qo_heads, c.level0.batch) == (4, 128, 1)
+    # merge input, request by request: 11 level-0 rows then the request's level-1 rows
+    assert c.merge_indptr.tolist() == [0, 12, 25, 38, 51]
+    assert c.l0_part_rows.tolist() == [0, 12, 25, 38]
+    # level-1 chunk j of request r lands at l1_part_rows[r] + j: chunks 0 | 1, 2 | 3, 4 | 5, 6
+    assert c.l1_part_rows.tolist() == [11, 22, 33, 44]
+
+
+def test_cascade_plan_brute_force():
+    """The chunk size and the merge layout against their definitions on random batches, members anywhere in
+    the level-1 table: the smallest size whose CTAs over both levels fit the wave; each request's rows are its
+    level-0 chunks (members) then its level-1 chunks; every row is written exactly once."""
+    rng = random.Random(11)
+    for _ in range(300):
+        B = rng.randint(1, 7)
+        M = rng.randint(1, B)
+        mreq = rng.sample(range(B), M)
+        Hkv = rng.choice([1, 2, 8])
+        G = rng.choice([1, 2, 4])
+        shared = rng.randint(1, 600)
+        pages = [rng.randint(1, 300) for _ in range(B)]
+        ip = [0]
+        for n in pages:
+            ip.append(ip[-1] + n)
+        wave = rng.randint(1, 400)
+        c = pa.pa_v2_cascade_plan(M, shared, ip, [16] * B, [0] * B, 16, Hkv * G, Hkv, 128, pa.PA_F16, wave,
+                                  member_requests=mreq)
+        hpc0 = min(M * G, 16)
+        per0, per1 = Hkv * -(-(M * G) // hpc0), Hkv
+
+        def ctas(k):
+            return per0 * -(-shared // k) + per1 * sum(max(1, -(-p // k)) for p in pages)
+        fits = [k for k in range(1, max(pages + [shared]) + 1) if ctas(k) <= wave]
+        want = min(fits) if fits else max(pages + [shared])
+        assert c.level0.pages_per_chunk == c.level1.pages_per_chunk == want
+        n0 = c.level0.num_chunks
+        o1 = c.level1.o_indptr.tolist()
+        rows = []
+        mi = c.merge_indptr.tolist()
+        for r in range(B):
+            mine = []
+            if r in mreq:
+                base = int(c.l0_part_rows[mreq.index(r)])
+                mine += [base + k for k in range(n0)]
+            mine += [int(c.l1_part_rows[r]) + j for j in range(o1[r], o1[r + 1])]
+            assert mine == list(range(mi[r], mi[r + 1])), (r, mine, mi)
+            rows += mine
+        assert rows == list(range(c.merge_rows))
+
+
+def test_cascade_plan_rejects_bad_arguments():
+    for args in ((0, 16), (2, 0), (3, 16)):          # no member, no shared page, more members than requests
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_v2_cascade_plan(*args, [0, 3, 5], [16, 16], [0, 0], 16, 32, 8, 128, pa.PA_F16, 152)
+        assert e.value.status == pa.PA_EINVAL
+    with pytest.raises(pa.PaError):
+        pa.pa_v2_cascade_plan(2, 16, [0, 3, 5], [16, 16], [0, 0], 16, 32, 8, 128, pa.PA_F16, 0)
+    with pytest.raises(pa.PaError):                   # a member listed twice
+        pa.pa_v2_cascade_plan(2, 16, [0, 3, 5], [16, 16], [0, 0], 16, 32, 8, 128, pa.PA_F16, 152,
+                              member_requests=[1, 1])
+
+
+def test_chunk_fit_helper():
     from paged_attention_decode_gb300 import cascade as C
-    # one wave of 152 split 2:1 by bytes; each level keeps at least one chunk's CTAs
-    assert C.split_wave(152, 2, 1, 8, 32) == (101, 51)
-    assert C.split_wave(152, 1000, 1, 8, 32) == (120, 32)
-    assert C.split_wave(152, 1, 1000, 8, 32) == (8, 144)
     # smallest chunk size whose CTAs fit the budget, by brute force
     rng = random.Random(3)
     for _ in range(300):

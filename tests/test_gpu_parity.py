@@ -101,20 +101,21 @@ def test_cascade_flat_and_two_level():
     assert float((co - flat_o).abs().max()) <= 2 * OUT_TOL
 
 
-@pytest.mark.parametrize("concurrent", [True, False])
-def test_cascade_driver_three_launches(concurrent):
-    """The library's cascade path (stacked level 0 read in place, rows interleaved for one merge); the two
-    levels on two streams sharing one wave, or one after the other on the caller's stream."""
+@pytest.mark.parametrize("wave", [0, 40, 1000])
+def test_cascade_driver_one_launch(wave):
+    """The library's cascade path (pa_v2_cascade_plan + pa_v2_cascade_decode: both levels in one launch of
+    the partial kernel, stacked level 0 read in place, rows interleaved for one merge); the device's wave
+    split between the levels, a small one (few, long chunks) and a large one (many short chunks)."""
     from paged_attention_decode_gb300 import cascade as C
     cb = W.cascade_shared_prefix()
     f = cb.flat
     dt = pa.KV_DTYPES[f.dtype]
     M, Hq, D = f.q.shape
-    t0 = pa.pa_v2_default_target_ctas(M * Hq, f.num_kv_heads, D, f.page_size, dt)
-    t1 = pa.pa_v2_default_target_ctas(Hq, f.num_kv_heads, D, f.page_size, dt)
     fp1 = torch.zeros(M, dtype=torch.int32)
     cp = C.cascade_plan(len(cb.prefix_indices), cb.suffix_indptr, cb.suffix_last_page_len, fp1, f.page_size, Hq,
-                        f.num_kv_heads, D, dt, t0, t1, cb.suffix_lens, concurrent=concurrent)
+                        f.num_kv_heads, D, dt, wave, cb.suffix_lens)
+    if wave:
+        assert cp.level0.total_ctas + cp.level1.total_ctas <= max(wave, 8 + 8 * M)
     dev = "cuda"
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     args = (f.q.to(dev), f.k_pool.to(dev), f.v_pool.to(dev), cb.prefix_indices.to(dev), cb.suffix_indices.to(dev),
@@ -129,14 +130,15 @@ def test_cascade_driver_three_launches(concurrent):
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
-@pytest.mark.parametrize("concurrent", [True, False])
-def test_cascade_on_a_mixed_batch(concurrent):
-    """Detection + split + three launches on a batch with members, a mid-page sharer and strangers."""
+@pytest.mark.parametrize("wave", [0, 24])
+def test_cascade_on_a_mixed_batch(wave):
+    """Detection + split + one two-level launch + merge on a batch with members, a mid-page sharer and
+    strangers (row maps for both levels)."""
     from paged_attention_decode_gb300 import cascade as C
     b = W.cascade_mixed_batch()
     dt = pa.KV_DTYPES[b.dtype]
     cp = C.plan_batch(b.indptr, b.indices, b.last_page_len, b.first_page_offset, b.page_size, b.num_qo_heads,
-                      b.num_kv_heads, b.head_dim, dt, concurrent=concurrent)
+                      b.num_kv_heads, b.head_dim, dt, wave_ctas=wave)
     assert cp is not None and cp.members == 3 and cp.shared_pages == b.meta["shared_pages"]
     d = b.to("cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
