@@ -564,9 +564,10 @@ PER_CONFIG = ("tiny_csr", "sliding_window_batch", "sparse_token_exact", "cascade
 
 
 def other_configs(args):
-    """us/step and KV-read GB/s of the other four workloads, each one step at a time after a 512 MiB read
-    (cold L2), median of 100 graph-replayed steps, each arm checked against the oracle first; the cascade
-    workload reports the cascade and the flat launch of the same batch."""
+    """us/step and KV-read GB/s of the other four workloads, each arm checked against the oracle first: one
+    step at a time after a 512 MiB read (cold L2), median of 100 graph-replayed steps, and (`steady`) steps
+    back to back over input variants whose K/V exceeds twice the L2; the cascade workload reports the cascade
+    and the flat launch of the same batch."""
     res = {}
     for name in PER_CONFIG:
         ns = argparse.Namespace(**vars(args))
@@ -580,6 +581,14 @@ def other_configs(args):
                  "pages_per_chunk": line["config"]["pages_per_chunk"], "num_chunks": line["config"]["num_chunks"],
                  "protocol": "cold L2 (512 MiB read before each step), one graph replay per step, median of 100",
                  "oracle_check": line["oracle_check"]}
+        st = line.get("steady")
+        if st:
+            entry["steady"] = {"us_per_step": st[main]["us_per_step"], "kv_read_gbs": st[main]["kv_read_gbs"],
+                               "pct_of_hbm_peak": 100.0 * st[main]["kv_read_gbs"] / line["hbm_peak_gbs"],
+                               "variants": st["variants"], "protocol": st["protocol"]}
+            if name == "cascade_shared_prefix":
+                entry["steady"]["flat_us_per_step"] = st["two"]["us_per_step"]
+                entry["steady"]["cascade_over_flat"] = st["cascade"]["us_per_step"] / st["two"]["us_per_step"]
         if name == "cascade_shared_prefix":
             entry["flat_us_per_step"] = arms["two"]["us_per_step_median"]
             entry["flat_logical_kv_bytes_per_step"] = arms["two"]["kv_bytes_per_step"]
@@ -915,6 +924,10 @@ def measure_workload(args):
         res[name] = {"us_per_step_median": med * 1e3, "us_p10": t[len(t) // 10] * 1e3,
                      "us_p90": t[(9 * len(t)) // 10] * 1e3, "kv_bytes_per_step": nbytes,
                      "kv_read_gbs": nbytes / (med * 1e-3) / 1e9}
+    steady = None
+    if args.workload != "tiny_csr":
+        steady = _steady(pa, b, cb, plan, d, dev, stream, cas_bytes if cascade else None,
+                         cplan if cascade else None)
     peak, peak_kind = measured_peak()
     main = res["cascade" if cascade else "two"]
     line = {"metric": "decode step us/step (median, cold L2) and KV-read GB/s", "value": main["us_per_step_median"],
@@ -928,12 +941,94 @@ def measure_workload(args):
                        "search_pages_per_chunk": search_ppc0,
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak,
-            "oracle_check": oracle_check}
+            "steady": steady, "oracle_check": oracle_check}
     if tuned is not None:
         line["autotune"] = {"pages_per_chunk": tuned.pages_per_chunk, "default": tuned.default_pages_per_chunk,
                             "times_us": {str(k): round(v, 2) for k, v in tuned.times_us.items()},
                             "num_chunks": {str(k): v for k, v in tuned.num_chunks.items()}}
     return line
+
+
+L2_BYTES = 126 << 20
+
+
+def _steady(pa, b, cb, plan, d, dev, stream, cas_bytes=None, cplan=None, reps=5):
+    """Steady-state steps: the step back to back, as a serving loop runs it, over variants of the input whose
+    K/V does not repeat within twice the L2 (each variant reads other memory: its page ids point into its own
+    copy of the pools, or, for the one-row pages of the sparse workload, at other rows of the same pool), from
+    a CUDA graph of several rotations; programmatic dependent launches let each step's kernels start while the
+    previous one finishes.  Returns per-step us and KV-read GB/s per arm ("two": partial + merge; "cascade")."""
+    from paged_attention_decode_gb300 import cascade as C
+    unique = cas_bytes if cas_bytes is not None else b.kv_bytes()
+    nsets = max(3, min(32, -(-2 * L2_BYTES // unique)))
+    P = b.k_pool.shape[0]
+    sparse = b.page_size == 1 and b.meta.get("cap")
+    if sparse:
+        cap = int(b.meta["cap"])
+        kp, vp = d.k_pool, d.v_pool
+        base = (d.indices // cap) * cap
+        pos = d.indices - base
+        idx = [base + (pos + 7919 * v) % cap for v in range(nsets)]
+    else:
+        kp = torch.cat([d.k_pool] * nsets)
+        vp = torch.cat([d.v_pool] * nsets)
+        idx = [d.indices + v * P for v in range(nsets)]
+    ri, ti, oi = plan.device_arrays(dev)
+    wv = torch.empty(max(1, plan.num_chunks), plan.num_qo_heads, plan.head_dim, device=dev)
+    wl = torch.empty(max(1, plan.num_chunks), plan.num_qo_heads, device=dev)
+    out = torch.empty(b.batch, b.num_qo_heads, b.head_dim, device=dev)
+    lse = torch.empty(b.batch, b.num_qo_heads, device=dev)
+
+    def two(v):
+        if plan.needs_merge:
+            pa.pa_v2_decode_partial(plan, d.q, kp, vp, idx[v], d.indptr, d.last_page_len, d.first_page_offset,
+                                    b.scale, wv, wl, None, stream, ri, ti)
+            pa.pa_merge_states(wv, wl, oi, b.batch, out, lse, None, stream)
+        else:
+            pa.pa_v2_decode_partial(plan, d.q, kp, vp, idx[v], d.indptr, d.last_page_len, d.first_page_offset,
+                                    b.scale, out, lse, None, stream, ri, ti)
+
+    arms = {"two": (two, b.kv_bytes())}
+    if cplan is not None:
+        pre = [cb.prefix_indices.to(dev) + v * P for v in range(nsets)]
+        suf = [cb.suffix_indices.to(dev) + v * P for v in range(nsets)]
+        sip, slp = cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev)
+        sfp = torch.zeros(len(cb.suffix_lens), dtype=torch.int32, device=dev)
+        c_out, c_lse = torch.empty_like(out), torch.empty_like(lse)
+
+        def casc(v):
+            C.cascade_decode(cplan, d.q, kp, vp, pre[v], suf[v], sip, slp, sfp, b.scale, out=c_out, lse2_out=c_lse,
+                             stream=stream)
+
+        arms["cascade"] = (casc, cas_bytes)
+    G = nsets * max(1, 60 // nsets)
+    res = {"variants": nsets, "steps_per_graph": G, "replays": reps,
+           "protocol": "back-to-back graph replays rotating over input variants whose K/V exceeds twice the L2"}
+    for name, (fn, nbytes) in arms.items():
+        with torch.cuda.stream(stream):
+            for v in range(nsets):
+                fn(v)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                fn(i % nsets)
+        with torch.cuda.stream(stream):
+            g.replay()
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(DELAY_CYCLES)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * G)
+        res[name] = {"us_per_step": us, "kv_bytes_per_step": nbytes, "kv_read_gbs": nbytes / (us * 1e-6) / 1e9}
+    del kp, vp
+    return res
 
 
 def _time_cold(fn, stream, flush, warmup, steps, graph):
