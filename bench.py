@@ -119,7 +119,10 @@ def measured_peak():
 
 
 KERNEL_SOURCES = {
-    "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_internal.cuh", "pa_device.cuh", "pa_mma.cuh"],
+    "pa_v2_partial_tc_kernel": ["pa_partial_tc.cu", "pa_partial_tc_body.cuh", "pa_internal.cuh", "pa_device.cuh",
+                                "pa_mma.cuh"],
+    "pa_v2_partial_tc_two_plan_kernel": ["pa_partial_tc_cascade.cu", "pa_partial_tc_body.cuh", "pa_internal.cuh",
+                                         "pa_device.cuh", "pa_mma.cuh"],
     "pa_v2_partial_simt_kernel": ["pa_partial_simt.cu", "pa_internal.cuh", "pa_device.cuh"],
     "pa_v2_partial_extra_tc05_kernel": ["pa_partial_extra_tc05.cu", "pa_internal.cuh", "pa_device.cuh", "pa_mma.cuh"],
 }
