@@ -1319,7 +1319,9 @@ def run_dsa(args):
         cells.append({"batch": B, "selected_rows_per_request": b.seq_lens[0], "chunks": plan.num_chunks,
                       "ctas": plan.total_ctas, "us_per_step_median": med, "us_p10": p10, "us_p90": p90,
                       "kv_bytes_per_step": nbytes, "kv_read_gbs": nbytes / (med * 1e-6) / 1e9,
-                      "flops_per_step": flops, "tflops": flops / (med * 1e-6) / 1e12})
+                      "flops_per_step": flops, "tflops": flops / (med * 1e-6) / 1e12,
+                      "gathered_bytes_per_step": nbytes * plan.q_groups,
+                      "gathered_gbs": nbytes * plan.q_groups / (med * 1e-6) / 1e9})
         del x, d, db
         torch.cuda.empty_cache()
     if args.profile:
@@ -1348,6 +1350,13 @@ def run_dsa(args):
                        "chunking": "smallest pages_per_chunk whose CTAs fit one wave, in whole 128-row tiles",
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "cells": cells, "roofline": roofline}
+    hpeak, hkind = measured_peak()
+    line["roofline_gather"] = {
+        "bound": "hbm", "achieved": big["gathered_gbs"], "peak": hpeak, "unit": "GB/s",
+        "frac": big["gathered_gbs"] / hpeak, "cell": f"batch {big['batch']}", "peak_source": f"{hkind} hbm_gbs",
+        "note": "bytes the CTAs gather (every selected row once per q-group CTA of its chunk) over the step time "
+                "against the HBM copy peak; one SM's intake of scattered rows, not DRAM bandwidth, bounds the "
+                "kernel"}
     print(json.dumps(line), flush=True)
 
 
