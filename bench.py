@@ -587,6 +587,7 @@ def other_configs(args):
         st = line.get("steady")
         if st:
             entry["steady"] = {"us_per_step": st[main]["us_per_step"], "kv_read_gbs": st[main]["kv_read_gbs"],
+                               "fused_us_per_step": st["fused"]["us_per_step"],
                                "pct_of_hbm_peak": 100.0 * st[main]["kv_read_gbs"] / line["hbm_peak_gbs"],
                                "variants": st["variants"], "protocol": st["protocol"]}
             if name == "cascade_shared_prefix":
@@ -960,7 +961,8 @@ def _steady(pa, b, cb, plan, d, dev, stream, cas_bytes=None, cplan=None, reps=5)
     K/V does not repeat within twice the L2 (each variant reads other memory: its page ids point into its own
     copy of the pools, or, for the one-row pages of the sparse workload, at other rows of the same pool), from
     a CUDA graph of several rotations; programmatic dependent launches let each step's kernels start while the
-    previous one finishes.  Returns per-step us and KV-read GB/s per arm ("two": partial + merge; "cascade")."""
+    previous one finishes.  Returns per-step us and KV-read GB/s per arm ("two": partial + merge; "fused": the
+    one-launch pa_v2_decode; "cascade")."""
     from paged_attention_decode_gb300 import cascade as C
     unique = cas_bytes if cas_bytes is not None else b.kv_bytes()
     nsets = max(3, min(32, -(-2 * L2_BYTES // unique)))
@@ -991,7 +993,13 @@ def _steady(pa, b, cb, plan, d, dev, stream, cas_bytes=None, cplan=None, reps=5)
             pa.pa_v2_decode_partial(plan, d.q, kp, vp, idx[v], d.indptr, d.last_page_len, d.first_page_offset,
                                     b.scale, out, lse, None, stream, ri, ti)
 
-    arms = {"two": (two, b.kv_bytes())}
+    counters = plan.device_counters(dev)
+
+    def fused(v):
+        pa.pa_v2_decode(plan, d.q, kp, vp, idx[v], d.indptr, d.last_page_len, d.first_page_offset, b.scale, out, lse,
+                        (wv, wl), counters, None, stream, ri, ti, oi)
+
+    arms = {"two": (two, b.kv_bytes()), "fused": (fused, b.kv_bytes())}
     if cplan is not None:
         pre = [cb.prefix_indices.to(dev) + v * P for v in range(nsets)]
         suf = [cb.suffix_indices.to(dev) + v * P for v in range(nsets)]
