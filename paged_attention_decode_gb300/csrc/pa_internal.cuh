@@ -208,44 +208,79 @@ __device__ __forceinline__ StageGeom stage_geom(const ChunkGeom& g, int j, int p
 // Merge the per-warp online-softmax states of a CTA of NW warps and write the
 // chunk's normalized output and lse2: to workspace row `row` (a chunk), or,
 // when final_output, to the final output of request `row`.  ms/ls:
-// [NW][HP]; accs: [NW][HP][D] (unnormalized, relative to each warp's max).
-// Called by all threads after a __syncthreads() that follows the state writes.
+// [NW][HP]; accs: [NW][HP] rows of DP >= D floats (unnormalized, relative to
+// each warp's max).  Called by all threads after a __syncthreads() that
+// follows the state writes.
+//
+// First one thread per head folds the warps' maxima into weights
+// 2^(m_w - M) (kept in ms in place) and stores 1/L and the lse in ls[0][h] and
+// ls[1][h]; then every thread combines float4 slices of the accumulators with
+// those weights.  ms and ls are consumed.
+// Query head h_first + h sits in state column h.
 // MAPPED: partial rows follow p.part_rows (the cascade launch); other launches compile without it.
-template <int HP, int D, int NW, bool MAPPED = false>
-__device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, const float* ms, const float* ls,
+template <int HP, int D, int NW, bool MAPPED = false, int DP = D>
+__device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, float* ms, float* ls,
                                                         const float* accs, int row, int h_first, int nheads,
                                                         bool final_output, int req = 0) {
-  for (int idx = threadIdx.x; idx < nheads * D; idx += NW * 32) {
-    const int h = idx / D;
-    const int d = idx % D;
+  static_assert(NW >= 2 && D % 4 == 0 && DP % 4 == 0, "float4 slices, two state rows for 1/L and lse");
+  constexpr int Q = D / 4;  // float4 slices per head row
+  const int tid = threadIdx.x;
+  if (tid < nheads) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * HP + h]);
-    float out = 0.f, lse = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * HP + tid]);
+    float inv = 0.f, lse = -INFINITY;
     if (M != -INFINITY) {
-      float L = 0.f, A = 0.f;
+      float L = 0.f;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        const float wgt = fast_exp2(ms[w * HP + h] - M);
-        L += ls[w * HP + h] * wgt;
-        A += accs[(w * HP + h) * D + d] * wgt;
+        const float wgt = fast_exp2(ms[w * HP + tid] - M);
+        ms[w * HP + tid] = wgt;
+        L += ls[w * HP + tid] * wgt;
       }
-      out = A / L;
+      inv = 1.f / L;
       lse = M + fast_log2(L);
-    }
-    if (final_output) {
-      const size_t o = out_row(p, row, h_first + h);
-      p.out[o * D + d] = out;
-      if (d == 0) p.lse_final[o] = lse;
-    } else if (MAPPED) {
-      const size_t o = part_row(p, row, req, h_first + h);
-      p.v_out[o * D + d] = out;
-      if (d == 0) p.lse_out[o] = lse;
     } else {
-      const size_t o = (size_t)row * p.num_qo_heads + h_first + h;
-      p.v_out[o * D + d] = out;
-      if (d == 0) p.lse_out[o] = lse;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) ms[w * HP + tid] = 0.f;
     }
+    ls[tid] = inv;
+    ls[HP + tid] = lse;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nheads * Q; idx += NW * 32) {
+    const int h = idx / Q;
+    const int q = idx % Q;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float wgt = ms[w * HP + h];
+      const float4 v = *reinterpret_cast<const float4*>(accs + (w * HP + h) * DP + 4 * q);
+      a.x = fmaf(v.x, wgt, a.x);
+      a.y = fmaf(v.y, wgt, a.y);
+      a.z = fmaf(v.z, wgt, a.z);
+      a.w = fmaf(v.w, wgt, a.w);
+    }
+    const float inv = ls[h];
+    const float4 o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    size_t orow;
+    float* dv;
+    float* dl;
+    if (final_output) {
+      orow = out_row(p, row, h_first + h);
+      dv = p.out;
+      dl = p.lse_final;
+    } else if (MAPPED) {
+      orow = part_row(p, row, req, h_first + h);
+      dv = p.v_out;
+      dl = p.lse_out;
+    } else {
+      orow = (size_t)row * p.num_qo_heads + h_first + h;
+      dv = p.v_out;
+      dl = p.lse_out;
+    }
+    reinterpret_cast<float4*>(dv + orow * D)[q] = o;
+    if (q == 0) dl[orow] = ls[HP + h];
   }
 }
 
@@ -385,9 +420,9 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, float* scrat
 // shared memory that is free once the states have been combined.
 // num_chunks, y, ny: the launch's chunk count, this CTA's row among the CTAs of a chunk and their number
 // (-1: the grid's own, gridDim.x, blockIdx.y, gridDim.y; a launch that runs two plans passes its plan's).
-template <int HP, int D, int NW, bool MAPPED = false>
-__device__ __forceinline__ void finish_chunk(const PartialParams& p, const ChunkGeom& g, const float* ms,
-                                             const float* ls, const float* accs, float* scratch, int c, int r,
+template <int HP, int D, int NW, bool MAPPED = false, int DP = D>
+__device__ __forceinline__ void finish_chunk(const PartialParams& p, const ChunkGeom& g, float* ms,
+                                             float* ls, const float* accs, float* scratch, int c, int r,
                                              int h_first, int nheads, int num_chunks = -1, int y = -1,
                                              int ny = -1) {
   if (MAPPED && g.bad) return;  // no row of a mapped workspace belongs to a chunk with a bad request
@@ -396,7 +431,7 @@ __device__ __forceinline__ void finish_chunk(const PartialParams& p, const Chunk
     const int n0 = p.o_indptr[r], n1 = p.o_indptr[r + 1];
     direct = n1 - n0 == 1;
   }
-  combine_warps_and_store<HP, D, NW, MAPPED>(p, ms, ls, accs, direct ? r : c, h_first, nheads, direct, r);
+  combine_warps_and_store<HP, D, NW, MAPPED, DP>(p, ms, ls, accs, direct ? r : c, h_first, nheads, direct, r);
   if (p.fused && !g.bad && !direct) {
     __syncthreads();  // scratch aliases the state arrays just read
     fused_merge<D, NW>(p, scratch, r, h_first, nheads, num_chunks < 0 ? (int)gridDim.x : num_chunks,

@@ -30,7 +30,8 @@ struct TcLayout {
   static constexpr int STAGE = 2 * TILE;
   static constexpr int STAGES_BYTES = NW * NSW * STAGE;
   static constexpr int PT_BYTES = NW * 2 * HP * 32;   // P^T hi/lo per warp: [HP][16] 16-bit
-  static constexpr int STATE_BYTES = NW * HP * D * 4;
+  static constexpr int DP = D + 4;                   // state row stride: 4 floats of padding per row
+  static constexpr int STATE_BYTES = NW * HP * DP * 4;
   static constexpr int BODY = STAGES_BYTES > STATE_BYTES ? STAGES_BYTES : STATE_BYTES;
   static constexpr int BARS = BODY + PT_BYTES;
   static constexpr int MS = BARS + NW * NSW * 8;
@@ -406,8 +407,9 @@ __device__ __forceinline__ void partial_tc_body(const CUtensorMap& tm_k, const C
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {
       const int h0 = 8 * jj + 2 * t;
-      float* a0 = accs + (warp * HP + h0) * D + 16 * mt + g;
-      float* a1 = a0 + D;
+      // rows DP = D + 4 floats apart: the four t-lanes writing rows h0 = 2t land in distinct banks
+      float* a0 = accs + (warp * HP + h0) * L::DP + 16 * mt + g;
+      float* a1 = a0 + L::DP;
       a0[0] = o[mt][jj][0];
       a1[0] = o[mt][jj][1];
       a0[8] = o[mt][jj][2];
@@ -424,7 +426,7 @@ __device__ __forceinline__ void partial_tc_body(const CUtensorMap& tm_k, const C
     }
   }
   __syncthreads();
-  finish_chunk<HP, D, NW, MAPPED>(p, gm, ms, ls, accs, accs, c, r, h_first, nheads, num_chunks, y, ny);
+  finish_chunk<HP, D, NW, MAPPED, L::DP>(p, gm, ms, ls, accs, accs, c, r, h_first, nheads, num_chunks, y, ny);
 }
 
 }  // namespace pa
