@@ -130,6 +130,35 @@ def test_cascade_driver_one_launch(wave):
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
+@pytest.mark.parametrize("ps,D,dt", [(5, 64, torch.bfloat16), (8, 128, torch.float16), (32, 64, torch.bfloat16),
+                                     (1, 128, torch.float16)])
+def test_cascade_staging_paths_and_head_dims(ps, D, dt):
+    """The two-level launch on every staging path of the tensor-core kernel: cp.async for page sizes TMA
+    cannot stage (5, 1), TMA boxes of whole 8-row pages and 16-row slices of 32-row pages; head_dim 64 and
+    128; against the oracle's cascade (levels + merge) and flat attention."""
+    from paged_attention_decode_gb300 import cascade as C
+    cb = W.cascade_shared_prefix(members=3, prefix_tokens=ps * (320 // ps), suffix_range=(3, 150), head_dim=D,
+                                 page_size=ps, dtype=dt, seed=70 + ps)
+    f = cb.flat
+    M, Hq, _ = f.q.shape
+    fp1 = torch.zeros(M, dtype=torch.int32)
+    cp = C.cascade_plan(len(cb.prefix_indices), cb.suffix_indptr, cb.suffix_last_page_len, fp1, ps, Hq,
+                        f.num_kv_heads, D, pa.KV_DTYPES[dt], 152, cb.suffix_lens)
+    dev = "cuda"
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = C.cascade_decode(cp, f.q.to(dev), f.k_pool.to(dev), f.v_pool.to(dev), cb.prefix_indices.to(dev),
+                                cb.suffix_indices.to(dev), cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev),
+                                fp1.to(dev), f.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.cascade_ref(f.q, f.k_pool, f.v_pool, cb.prefix_indices, cb.suffix_indices,
+                                      cb.suffix_indptr, cb.suffix_last_page_len, f.scale)
+    assert_close(out, lse, ref_o, ref_l, f"cascade ps={ps} D={D}")
+    flat_o, flat_l = oracle.attention(f.q, f.k_pool, f.v_pool, f.indices, f.indptr, f.last_page_len,
+                                      f.first_page_offset, f.scale)
+    assert_close(out, lse, flat_o, flat_l, f"cascade vs flat ps={ps} D={D}")
+
+
 @pytest.mark.parametrize("wave", [0, 24])
 def test_cascade_on_a_mixed_batch(wave):
     """Detection + split + one two-level launch + merge on a batch with members, a mid-page sharer and
