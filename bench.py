@@ -502,11 +502,16 @@ def run_ours(args):
     # the other four workloads, each checked against the oracle before it is timed
     per_config = None
     if rank == 0 and not args.no_per_config:
+        peak_gbs = measured_peak()[0]
         per_config = {"llama3_8b_32k": {
-            "us_per_step": ms_step * 1e3, "protocol": "the timed steps above (graph replays, rotating sets)",
-            "cold_l2_median_us": cold_med, "kv_bytes_per_step": kv_bytes,
-            "kv_read_gbs": kv_bytes / (ms_step * 1e-3) / 1e9,
-            "pct_of_hbm_peak": 100.0 * kv_bytes / (ms_step * 1e-3) / 1e9 / measured_peak()[0],
+            "steady": {"us_per_step": ms_step * 1e3, "kv_read_gbs": kv_bytes / (ms_step * 1e-3) / 1e9,
+                       "pct_of_hbm_peak": 100.0 * kv_bytes / (ms_step * 1e-3) / 1e9 / peak_gbs,
+                       "protocol": "the timed steps above (graph replays, rotating sets)"},
+            "cold": {"us_per_step": cold_med, "p10_us": cold_p10, "p90_us": cold_p90,
+                     "kv_read_gbs": kv_bytes / (cold_med * 1e-6) / 1e9,
+                     "pct_of_hbm_peak": 100.0 * kv_bytes / (cold_med * 1e-6) / 1e9 / peak_gbs,
+                     "protocol": "per_step_cold_l2"},
+            "kv_bytes_per_step": kv_bytes, "pages_per_chunk": plan.pages_per_chunk, "num_chunks": N,
             "oracle_check": {"max_abs_out": err}}}
         per_config.update(other_configs(args))
 
@@ -578,25 +583,30 @@ def other_configs(args):
         line = measure_workload(ns)
         arms = line["arms"]
         main = "cascade" if name == "cascade_shared_prefix" else "two"
-        entry = {"us_per_step": arms[main]["us_per_step_median"], "p10_us": arms[main]["us_p10"],
-                 "p90_us": arms[main]["us_p90"], "kv_bytes_per_step": arms[main]["kv_bytes_per_step"],
-                 "kv_read_gbs": arms[main]["kv_read_gbs"], "pct_of_hbm_peak": line["pct_of_hbm_peak"],
-                 "pages_per_chunk": line["config"]["pages_per_chunk"], "num_chunks": line["config"]["num_chunks"],
-                 "protocol": "cold L2 (512 MiB read before each step), one graph replay per step, median of 100",
-                 "oracle_check": line["oracle_check"]}
+        peak_gbs = line["hbm_peak_gbs"]
+        nbytes = arms[main]["kv_bytes_per_step"]
+        entry = {"cold": {"us_per_step": arms[main]["us_per_step_median"], "p10_us": arms[main]["us_p10"],
+                          "p90_us": arms[main]["us_p90"], "kv_read_gbs": arms[main]["kv_read_gbs"],
+                          "pct_of_hbm_peak": line["pct_of_hbm_peak"],
+                          "protocol": "512 MiB read before each step, one graph replay per step, median of 100"},
+                 "kv_bytes_per_step": nbytes, "pages_per_chunk": line["config"]["pages_per_chunk"],
+                 "num_chunks": line["config"]["num_chunks"], "oracle_check": line["oracle_check"]}
         st = line.get("steady")
         if st:
             entry["steady"] = {"us_per_step": st[main]["us_per_step"], "kv_read_gbs": st[main]["kv_read_gbs"],
-                               "fused_us_per_step": st["fused"]["us_per_step"],
-                               "pct_of_hbm_peak": 100.0 * st[main]["kv_read_gbs"] / line["hbm_peak_gbs"],
-                               "variants": st["variants"], "protocol": st["protocol"]}
-            if name == "cascade_shared_prefix":
+                               "pct_of_hbm_peak": 100.0 * st[main]["kv_read_gbs"] / peak_gbs,
+                               "fused_us_per_step": st["fused"]["us_per_step"], "variants": st["variants"],
+                               "protocol": st["protocol"]}
+        if name == "cascade_shared_prefix":
+            entry["flat_pages_per_chunk"] = entry.pop("pages_per_chunk")
+            entry["flat_num_chunks"] = entry.pop("num_chunks")
+            entry["cascade_plan"] = line["config"]["cascade"]
+            entry["cold"]["flat_us_per_step"] = arms["two"]["us_per_step_median"]
+            entry["cold"]["cascade_over_flat"] = arms["cascade"]["us_per_step_median"] / arms["two"]["us_per_step_median"]
+            entry["flat_logical_kv_bytes_per_step"] = arms["two"]["kv_bytes_per_step"]
+            if st:
                 entry["steady"]["flat_us_per_step"] = st["two"]["us_per_step"]
                 entry["steady"]["cascade_over_flat"] = st["cascade"]["us_per_step"] / st["two"]["us_per_step"]
-        if name == "cascade_shared_prefix":
-            entry["flat_us_per_step"] = arms["two"]["us_per_step_median"]
-            entry["flat_logical_kv_bytes_per_step"] = arms["two"]["kv_bytes_per_step"]
-            entry["cascade_over_flat"] = arms["cascade"]["us_per_step_median"] / arms["two"]["us_per_step_median"]
         res[name] = entry
     return res
 
@@ -946,6 +956,11 @@ def measure_workload(args):
                        "l2": "512 MiB buffer read between steps", "cuda_graph": bool(args.graph)},
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak,
             "steady": steady, "oracle_check": oracle_check}
+    if cascade:
+        line["config"]["cascade"] = {"pages_per_chunk": cplan.level0.pages_per_chunk,
+                                     "level0_chunks": cplan.level0.num_chunks, "level1_chunks": cplan.level1.num_chunks,
+                                     "ctas": cplan.level0.total_ctas + cplan.level1.total_ctas,
+                                     "merge_rows": cplan.plans.merge_rows}
     if tuned is not None:
         line["autotune"] = {"pages_per_chunk": tuned.pages_per_chunk, "default": tuned.default_pages_per_chunk,
                             "times_us": {str(k): round(v, 2) for k, v in tuned.times_us.items()},
