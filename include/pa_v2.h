@@ -322,7 +322,9 @@ pa_status pa_v2_cascade_plan(int32_t members, int32_t shared_pages, const int32_
  * member m, or null for m) and part_rows: the merge-input row of the level's
  * first chunk of each request (member, for level 0), so that chunk c of
  * request r lands in row part_rows[r] + c (pa_v2_cascade_plan computes both
- * levels' part_rows).  DEVICE pointers, owned by the caller. */
+ * levels' part_rows; a row at or past merge_rows is not written and sets
+ * PA_DEVICE_BAD_INDPTR in the status word).  DEVICE pointers, owned by the
+ * caller. */
 typedef struct pa_v2_cascade_level_t {
     const int32_t* indices;
     int64_t num_indices;

@@ -48,6 +48,7 @@ struct PartialParams {
   // part_rows[r] + c instead of row c, heads in member layout when stacked (one merge input holding
   // both cascade levels' chunks of each request, contiguously)
   const int32_t* part_rows;
+  int64_t part_limit;          // rows x heads of the mapped workspace: a mapped row past it is skipped
   int64_t num_pages;
   int64_t num_indices;
   int32_t single_pages;  // > 0: a one-request plan of this many pages (chunk c is tile c of request 0)
@@ -274,6 +275,10 @@ __device__ __forceinline__ void combine_warps_and_store(const PartialParams& p, 
       orow = part_row(p, row, req, h_first + h);
       dv = p.v_out;
       dl = p.lse_out;
+      if (orow >= (size_t)p.part_limit) {  // a row map pointing past the merge input: record, do not write
+        report(p.status, PA_DEVICE_BAD_INDPTR);
+        continue;
+      }
     } else {
       orow = (size_t)row * p.num_qo_heads + h_first + h;
       dv = p.v_out;

@@ -307,6 +307,7 @@ extern "C" pa_status pa_v2_cascade_decode(const pa_v2_plan_t* plan0, const pa_v2
                        &tk[l], &tv[l], &tc[l], &tma[l]);
     if (rc != PA_OK) return rc;
     a[l].p.part_rows = lv[l]->part_rows;
+    a[l].p.part_limit = (int64_t)merge_rows * plan1->num_qo_heads;
     a[l].p.member_rows = lv[l]->member_rows;
   }
   if (a[0].num_chunks == 0 || a[1].num_chunks == 0) return PA_EINVAL;  // each level has at least one chunk

@@ -159,6 +159,35 @@ def test_cascade_staging_paths_and_head_dims(ps, D, dt):
     assert_close(out, lse, flat_o, flat_l, f"cascade vs flat ps={ps} D={D}")
 
 
+def test_cascade_row_map_past_the_merge_input_is_refused_on_the_device():
+    """A part_rows entry pointing past the merge input: the kernel writes nothing there and records
+    PA_DEVICE_BAD_INDPTR (the host cannot see device row maps)."""
+    cb = W.cascade_shared_prefix(members=2, prefix_tokens=256, suffix_range=(20, 40))
+    f = cb.flat
+    M, Hq, D = f.q.shape
+    dt = pa.KV_DTYPES[f.dtype]
+    cps = pa.pa_v2_cascade_plan(M, len(cb.prefix_indices), cb.suffix_indptr, cb.suffix_last_page_len,
+                                torch.zeros(M, dtype=torch.int32), f.page_size, Hq, f.num_kv_heads, D, dt, 152)
+    dev = "cuda"
+    pr0 = cps.l0_part_rows.clone()
+    pr0[0] = cps.merge_rows + 1000
+    merge_v = torch.zeros(cps.merge_rows, Hq, D, device=dev)
+    merge_l = torch.zeros(cps.merge_rows, Hq, device=dev)
+    canary = torch.full((4096,), 5.0, device=dev)   # allocated after the merge input
+    lv0 = pa.cascade_level(cps.level0, cb.prefix_indices.to(dev), torch.tensor([0, len(cb.prefix_indices)],
+                           dtype=torch.int32, device=dev), torch.tensor([f.page_size], dtype=torch.int32, device=dev),
+                           torch.zeros(1, dtype=torch.int32, device=dev), pr0.to(dev))
+    lv1 = pa.cascade_level(cps.level1, cb.suffix_indices.to(dev), cb.suffix_indptr.to(dev),
+                           cb.suffix_last_page_len.to(dev), torch.zeros(M, dtype=torch.int32, device=dev),
+                           cps.l1_part_rows.to(dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pa.pa_v2_cascade_decode(cps, lv0, lv1, f.q.to(dev), f.k_pool.to(dev), f.v_pool.to(dev), f.scale, merge_v, merge_l,
+                            cps.merge_indptr.to(dev), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & pa.DEVICE_BAD_INDPTR
+    assert bool((canary == 5.0).all())
+
+
 @pytest.mark.parametrize("wave", [0, 24])
 def test_cascade_on_a_mixed_batch(wave):
     """Detection + split + one two-level launch + merge on a batch with members, a mid-page sharer and
