@@ -666,18 +666,22 @@ def compare_chunkings(args, pa, alt_ppc, sets, b0, dt, target, dev, stream, step
 
 def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     """Per step, one call of the C ABI with host buffers: pa_v2_host_graph_run through the binding's
-    HostStep -- the cached plan checked against the step's page table, then one graph launch holding the
-    host-to-device copy of q and the page table from pinned memory, the partial and merge launches and the
-    device-to-host copy of out, lse2 and the status word -- and stream synchronisation.  The same step as
-    one direct pa_v2_decode_host call is timed beside it.  The fused one-launch step (--fused) keeps the
-    per-array path: pa_v2_plan_matches, a pinned copy, pa_v2_decode, a copy back."""
+    HostStep on a graph from pa_v2_host_graph_create_mapped -- the cached plan checked against the step's
+    page table, the status slot zeroed, one graph launch whose partial kernel reads q and the page table
+    from pinned host memory over NVLink-C2C and whose merge writes out and lse2 back into pinned host
+    memory -- and stream synchronisation.  Timed beside it: the same step as one direct
+    pa_v2_decode_host_mapped call, and both again with copy-engine copies (pa_v2_host_graph_create /
+    pa_v2_decode_host: one pinned H2D of the packed inputs into a device buffer, one D2H of the outputs).
+    The fused one-launch step (--fused) keeps the per-array path: pa_v2_plan_matches, a pinned copy,
+    pa_v2_decode, a copy back."""
     if args.fused:
         return run_e2e_fused(args, pa, plan, sets_cpu, sets, dev, stream, b0)
 
-    def timed(graph):
+    def timed(graph, mapped):
         steps = []
         for b, d in zip(sets_cpu, sets):
-            st = pa.HostStep(plan, d.k_pool, d.v_pool, stream, graph_scale=b0.scale if graph else None)
+            st = pa.HostStep(plan, d.k_pool, d.v_pool, stream, graph_scale=b0.scale if graph else None,
+                             mapped=mapped)
             st.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
             steps.append(st)
         for i in range(20):
@@ -686,17 +690,29 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
         t0 = time.perf_counter()
         for i in range(n):
             steps[i % len(steps)].run(b0.scale)
-        return (time.perf_counter() - t0) / n, steps[0]
+        el = (time.perf_counter() - t0) / n
+        o = steps[(n - 1) % len(steps)].out.clone()
+        return el, steps[0], o
 
-    direct_s, _ = timed(False)
-    per_step, st0 = timed(True)
+    copy_direct, _, _ = timed(False, False)
+    copy_graph, _, o_copy = timed(True, False)
+    mapped_direct, _, _ = timed(False, True)
+    per_step, st0, o_mapped = timed(True, True)
+    if not torch.equal(o_copy, o_mapped):
+        raise RuntimeError("mapped and copied host steps disagree")
     kv_bytes = b0.kv_bytes()
     return {"value": kv_bytes / per_step / 1e9, "unit": "GB/s", "us_per_step": per_step * 1e6,
-            "steps": args.e2e_steps, "h2d_bytes_per_step": st0.in_bytes, "d2h_bytes_per_step": st0.out_bytes,
-            "direct_call_us_per_step": direct_s * 1e6,
-            "path": "per step: pa_v2_host_graph_run (plan check against the step's page table, one graph launch: "
-                    "1 pinned H2D of q + page table, " + STEP_TWO + ", 1 D2H of status + out + lse2; stream sync); "
-                    "direct_call_us_per_step: the same step as one pa_v2_decode_host call"}
+            "steps": args.e2e_steps, "h2d_bytes_per_step": st0.in_bytes - 16, "d2h_bytes_per_step": st0.out_bytes,
+            "direct_call_us_per_step": mapped_direct * 1e6,
+            "copy_engine": {"graph_us_per_step": copy_graph * 1e6, "direct_call_us_per_step": copy_direct * 1e6,
+                            "h2d_bytes_per_step": st0.in_bytes, "d2h_bytes_per_step": st0.out_bytes},
+            "path": "per step: pa_v2_host_graph_run on a pa_v2_host_graph_create_mapped graph (plan check "
+                    "against the step's page table, status slot zeroed, one graph launch: " + STEP_TWO +
+                    " with q and the page table read by the partial kernel from pinned host memory over "
+                    "NVLink-C2C and status + out + lse2 written by the merge into pinned host memory; stream "
+                    "sync); direct_call_us_per_step: the same step as one pa_v2_decode_host_mapped call; "
+                    "copy_engine: the same step with one H2D copy of the packed inputs and one D2H copy of "
+                    "the outputs (pa_v2_host_graph_create / pa_v2_decode_host)"}
 
 
 def run_e2e_fused(args, pa, plan, sets_cpu, sets, dev, stream, b0):

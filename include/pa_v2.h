@@ -516,6 +516,39 @@ pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const void* host_in,
 pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* graph, void* cuda_stream);
 void pa_v2_host_graph_destroy(pa_v2_host_graph_t* graph);
 
+/* The same step with no copies, for a GPU that reaches host memory directly
+ * (on a GB300, the Grace CPU's memory over the coherent NVLink-C2C link).
+ * host_in and host_out keep the pa_v2_host_io_layout layout but must be
+ * page-locked and mapped into the device's address space (cudaHostAlloc, or
+ * cudaHostRegister with cudaHostRegisterMapped) and 16-byte aligned; the
+ * partial kernel reads q and the page table from host_in through its device
+ * address, and the last kernel writes out and lse2 into host_out, whose first
+ * 16 bytes are the status slot: the call (or run()) zeroes it from the host
+ * before the launch, and the kernels OR their error bits into it.  host_in's
+ * trailing status slot is not used, and there is no dev_io.
+ *
+ * pa_v2_decode_host_mapped: check the plan against host_in's page table
+ * (PA_EGEOMETRY, nothing launched), launch the partial kernel and the merge
+ * when plan->needs_merge, synchronize cuda_stream and return
+ * pa_status_from_device of the status word.  PA_EINVAL as pa_v2_decode_host,
+ * and when host_in or host_out is unaligned or has no device mapping.
+ *
+ * pa_v2_host_graph_create_mapped: capture the same two launches as a graph,
+ * bound like pa_v2_host_graph_create; pa_v2_host_graph_run and
+ * pa_v2_host_graph_destroy serve both kinds of graph.  Neither host buffer may
+ * be written while a step that uses it runs (between the launch and the
+ * synchronisation that ends it). */
+pa_status pa_v2_decode_host_mapped(const pa_v2_plan_t* plan, const void* host_in, void* host_out, const void* k_pool,
+                                   const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                   const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                   const int32_t* o_indptr, float sm_scale, float* workspace_v, float* workspace_lse,
+                                   void* cuda_stream);
+pa_status pa_v2_host_graph_create_mapped(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
+                                         const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                                         const int32_t* request_indices, const int32_t* kv_tile_indices,
+                                         const int32_t* o_indptr, float sm_scale, float* workspace_v,
+                                         float* workspace_lse, pa_v2_host_graph_t** graph);
+
 /* Size of the device scratch array behind pa_v2_decode_noalloc: 8 MiB, held
  * by every GPU that loads this library until the process exits. */
 #define PA_V2_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -10,6 +10,14 @@
 // several API calls per step; here the inputs travel as one packed buffer in
 // one host-to-device copy and the outputs (with the device status word) in one
 // device-to-host copy, on the caller's stream.
+//
+// The mapped variants drop both copies.  On a GB300 the Grace CPU's memory is
+// reachable from the GPU over the coherent NVLink-C2C link, so the kernels read
+// the packed inputs straight out of the caller's page-locked host_in and the
+// last kernel writes the status, out and lse2 straight into host_out: each step
+// is then two kernel launches, the second a programmatic dependent of the first,
+// instead of copy -> partial -> merge -> copy with a full dependency at either
+// copy.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,17 +45,33 @@ extern "C" pa_status pa_v2_host_io_layout(const pa_v2_plan_t* plan, int64_t* in_
 
 namespace {
 
+// The device address of a page-locked, mapped host buffer (16-byte aligned), or
+// null.
+unsigned char* mapped_address(const void* host) {
+  if (!host || (reinterpret_cast<uintptr_t>(host) & 15u)) return nullptr;
+  void* dev = nullptr;
+  if (cudaHostGetDevicePointer(&dev, const_cast<void*>(host), 0) != cudaSuccess || !dev) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned char*>(dev);
+}
+
 // Queue one host step on `stream` without waiting: the input copy, the partial
 // kernel (and the merge when the plan needs one), the output copy.  Checks the
-// arguments and the plan against the step's page table first.
+// arguments and the plan against the step's page table first.  With `mapped`
+// (the device addresses of host_in and host_out, from mapped_address): no
+// copies; the kernels read and write those, the status word is host_out's,
+// which the caller zeroes before the step, and dev_io is not used.
 pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
                             const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
                             const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
                             float sm_scale, float* workspace_v, float* workspace_lse, cudaStream_t stream,
-                            bool check_geometry) {
+                            bool check_geometry, unsigned char* const* mapped) {
   int64_t in_bytes = 0, out_bytes = 0, io_bytes = 0;
   if (pa_v2_host_io_layout(plan, &in_bytes, &out_bytes, &io_bytes) != PA_OK) return PA_EINVAL;
-  if (!host_in || !host_out || !dev_io || (reinterpret_cast<uintptr_t>(dev_io) & 15u)) return PA_EINVAL;
+  if (!host_in || !host_out) return PA_EINVAL;
+  if (!mapped && (!dev_io || (reinterpret_cast<uintptr_t>(dev_io) & 15u))) return PA_EINVAL;
   if (plan->needs_merge && (!workspace_v || !workspace_lse || !o_indptr)) return PA_EINVAL;
   const int32_t B = plan->batch;
   const int64_t rows = (int64_t)B * plan->num_qo_heads;
@@ -60,15 +84,25 @@ pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void*
   const int32_t* h_fpo = h_lpl + B;
   if (check_geometry && !pa_v2_plan_matches(plan, h_indptr, h_lpl, h_fpo, B)) return PA_EGEOMETRY;
 
-  unsigned char* io = static_cast<unsigned char*>(dev_io);
-  if (cudaMemcpyAsync(io, host_in, (size_t)in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return PA_ECUDA;
+  const unsigned char* in_region;  // the packed inputs as the kernels address them
+  unsigned char* out_region;       // the status slot, then out, lse2
+  if (mapped) {
+    in_region = mapped[0];
+    out_region = mapped[1];
+    if (!in_region || !out_region) return PA_EINVAL;
+  } else {
+    unsigned char* io = static_cast<unsigned char*>(dev_io);
+    in_region = io;
+    if (cudaMemcpyAsync(io, host_in, (size_t)in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return PA_ECUDA;
+    out_region = io + in_bytes - 16;  // the status slot the copy above zeroed
+  }
 
-  const float* q = reinterpret_cast<const float*>(io);
-  const int32_t* indices = reinterpret_cast<const int32_t*>(io) + q_words;
+  const float* q = reinterpret_cast<const float*>(in_region);
+  const int32_t* indices = reinterpret_cast<const int32_t*>(in_region) + q_words;
   const int32_t* indptr = indices + plan->num_indices;
   const int32_t* lpl = indptr + B + 1;
   const int32_t* fpo = lpl + B;
-  unsigned char* out_region = io + in_bytes - 16;  // the status slot the copy above zeroed, then out, lse2
   int32_t* status = reinterpret_cast<int32_t*>(out_region);
   float* out = reinterpret_cast<float*>(out_region + 16);
   float* lse = out + q_words;
@@ -86,9 +120,36 @@ pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void*
                               fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cs);
   }
   if (rc != PA_OK) return rc;
-  if (cudaMemcpyAsync(host_out, out_region, (size_t)out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  if (!mapped &&
+      cudaMemcpyAsync(host_out, out_region, (size_t)out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return PA_ECUDA;
   return PA_OK;
+}
+
+void clear_status_slot(void* host_out) { std::memset(host_out, 0, 16); }
+
+pa_status decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                      const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                      const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                      float sm_scale, float* workspace_v, float* workspace_lse, void* cuda_stream, bool mapped) {
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  unsigned char* addr[2] = {nullptr, nullptr};
+  if (mapped) {
+    addr[0] = mapped_address(host_in);
+    addr[1] = mapped_address(host_out);
+    if (addr[1]) clear_status_slot(host_out);
+  }
+  const pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
+                                         request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v,
+                                         workspace_lse, stream, true, mapped ? addr : nullptr);
+  if (rc != PA_OK) {
+    cudaStreamSynchronize(stream);  // a copy or kernel already queued may still be reading host_in
+    return rc;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
+  int32_t word = 0;
+  std::memcpy(&word, host_out, sizeof(word));
+  return pa_status_from_device(word);
 }
 
 }  // namespace
@@ -98,18 +159,18 @@ extern "C" pa_status pa_v2_decode_host(const pa_v2_plan_t* plan, const void* hos
                                        const int32_t* request_indices, const int32_t* kv_tile_indices,
                                        const int32_t* o_indptr, float sm_scale, float* workspace_v,
                                        float* workspace_lse, void* cuda_stream) {
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  const pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
-                                         request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v,
-                                         workspace_lse, stream, true);
-  if (rc != PA_OK) {
-    cudaStreamSynchronize(stream);  // the input copy may still be reading host_in
-    return rc;
-  }
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
-  int32_t word = 0;
-  std::memcpy(&word, host_out, sizeof(word));
-  return pa_status_from_device(word);
+  return decode_host(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages, request_indices,
+                     kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse, cuda_stream, false);
+}
+
+extern "C" pa_status pa_v2_decode_host_mapped(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
+                                              const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                                              int64_t num_pages, const int32_t* request_indices,
+                                              const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                                              float sm_scale, float* workspace_v, float* workspace_lse,
+                                              void* cuda_stream) {
+  return decode_host(plan, host_in, host_out, nullptr, k_pool, v_pool, kv_dtype, num_pages, request_indices,
+                     kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse, cuda_stream, true);
 }
 
 // ---- the same step as one CUDA graph ---------------------------------------
@@ -125,17 +186,27 @@ struct pa_v2_host_graph {
   pa_v2_plan_t plan;
   const void* host_in;
   void* host_out;
+  bool mapped;  // the status slot is host_out's, zeroed by run()
   cudaGraph_t graph;
   cudaGraphExec_t exec;
 };
 
-extern "C" pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
-                                             void* dev_io, const void* k_pool, const void* v_pool, int32_t kv_dtype,
-                                             int64_t num_pages, const int32_t* request_indices,
-                                             const int32_t* kv_tile_indices, const int32_t* o_indptr, float sm_scale,
-                                             float* workspace_v, float* workspace_lse, pa_v2_host_graph_t** out) {
+namespace {
+
+pa_status host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
+                            const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
+                            const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                            float sm_scale, float* workspace_v, float* workspace_lse, bool mapped,
+                            pa_v2_host_graph_t** out) {
   if (!plan || !out) return PA_EINVAL;
   *out = nullptr;
+  // resolved before the capture, which admits only stream work
+  unsigned char* addr[2] = {nullptr, nullptr};
+  if (mapped) {
+    addr[0] = mapped_address(host_in);
+    addr[1] = mapped_address(host_out);
+    if (!addr[0] || !addr[1]) return PA_EINVAL;
+  }
   cudaStream_t cap = nullptr;
   if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return PA_ECUDA;
   if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
@@ -145,7 +216,7 @@ extern "C" pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const voi
   // the geometry is checked on every run, against that step's page table
   pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
                                    request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse,
-                                   cap, false);
+                                   cap, false, mapped ? addr : nullptr);
   cudaGraph_t graph = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
   cudaStreamDestroy(cap);
@@ -161,10 +232,32 @@ extern "C" pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const voi
   g->plan = *plan;
   g->host_in = host_in;
   g->host_out = host_out;
+  g->mapped = mapped;
   g->graph = graph;
   g->exec = exec;
   *out = g;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_v2_host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
+                                             void* dev_io, const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                                             int64_t num_pages, const int32_t* request_indices,
+                                             const int32_t* kv_tile_indices, const int32_t* o_indptr, float sm_scale,
+                                             float* workspace_v, float* workspace_lse, pa_v2_host_graph_t** out) {
+  return host_graph_create(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages, request_indices,
+                           kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse, false, out);
+}
+
+extern "C" pa_status pa_v2_host_graph_create_mapped(const pa_v2_plan_t* plan, const void* host_in, void* host_out,
+                                                    const void* k_pool, const void* v_pool, int32_t kv_dtype,
+                                                    int64_t num_pages, const int32_t* request_indices,
+                                                    const int32_t* kv_tile_indices, const int32_t* o_indptr,
+                                                    float sm_scale, float* workspace_v, float* workspace_lse,
+                                                    pa_v2_host_graph_t** out) {
+  return host_graph_create(plan, host_in, host_out, nullptr, k_pool, v_pool, kv_dtype, num_pages, request_indices,
+                           kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse, true, out);
 }
 
 extern "C" pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* g, void* cuda_stream) {
@@ -174,6 +267,7 @@ extern "C" pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* g, void* cuda_stre
   const int32_t* h_words = static_cast<const int32_t*>(g->host_in);
   const int32_t* h_indptr = h_words + (int64_t)B * plan->num_qo_heads * plan->head_dim + plan->num_indices;
   if (!pa_v2_plan_matches(plan, h_indptr, h_indptr + B + 1, h_indptr + 2 * B + 1, B)) return PA_EGEOMETRY;
+  if (g->mapped) clear_status_slot(g->host_out);
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   if (cudaGraphLaunch(g->exec, stream) != cudaSuccess) {
     cudaStreamSynchronize(stream);

@@ -34,7 +34,8 @@ ABI_SYMBOLS = ("pa_v2_q_heads_per_cta", "pa_v2_default_target_ctas", "pa_v2_plan
                "pa_v2_cascade_detect", "pa_v2_cascade_split", "pa_selection_rows_per_request", "pa_sparse_csr",
                "pa_selection_from_blocks", "pa_v2_host_io_layout", "pa_v2_decode_host",
                "pa_v2_decode_partial_extra", "pa_v2_selftest_wait", "pa_v2_host_graph_create",
-               "pa_v2_host_graph_run", "pa_v2_host_graph_destroy", "pa_v2_wave_fit_pages_per_chunk",
+               "pa_v2_host_graph_run", "pa_v2_host_graph_destroy", "pa_v2_decode_host_mapped",
+               "pa_v2_host_graph_create_mapped", "pa_v2_wave_fit_pages_per_chunk",
                "pa_v2_balanced_pages_per_chunk", "pa_v2_cascade_plan", "pa_v2_cascade_decode",
                "pa_status_from_device", "pa_status_string", "pa_version")
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -116,6 +117,10 @@ def lib() -> ctypes.CDLL:
         L.pa_v2_selftest_wait.restype = i32
         L.pa_v2_host_graph_create.argtypes = [PP, P, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
         L.pa_v2_host_graph_create.restype = i32
+        L.pa_v2_decode_host_mapped.argtypes = [PP, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
+        L.pa_v2_decode_host_mapped.restype = i32
+        L.pa_v2_host_graph_create_mapped.argtypes = [PP, P, P, P, P, i32, i64, P, P, P, f32, P, P, P]
+        L.pa_v2_host_graph_create_mapped.restype = i32
         L.pa_v2_host_graph_run.argtypes = [P, P]
         L.pa_v2_host_graph_run.restype = i32
         L.pa_v2_host_graph_destroy.argtypes = [P]
@@ -617,16 +622,19 @@ class HostStep:
     input buffer (or pass prepacked=True to run() after filling `host_in` yourself); run() makes the one
     C call and returns (out [B, Hq, D], lse2 [B, Hq]) as views of the pinned output buffer.
     graph_scale: also capture the step as a CUDA graph (pa_v2_host_graph_create) bound to this scale;
-    run() with that scale then replays it (pa_v2_host_graph_run)."""
+    run() with that scale then replays it (pa_v2_host_graph_run).
+    mapped: the copy-free calls (pa_v2_decode_host_mapped / pa_v2_host_graph_create_mapped): the kernels
+    read host_in and write host_out through their device mappings, and there is no device io buffer."""
 
-    def __init__(self, plan: Plan, k_pool, v_pool, stream=None, graph_scale=None):
+    def __init__(self, plan: Plan, k_pool, v_pool, stream=None, graph_scale=None, mapped: bool = False):
         s = plan.struct
         self.plan = plan
         dev = k_pool.device
         self.in_bytes, self.out_bytes, self.io_bytes = pa_v2_host_io_layout(plan)
         self.host_in = torch.zeros(self.in_bytes, dtype=torch.uint8).pin_memory()
         self.host_out = torch.zeros(self.out_bytes, dtype=torch.uint8).pin_memory()
-        self.dev_io = torch.empty(self.io_bytes, dtype=torch.uint8, device=dev)
+        self.mapped = bool(mapped)
+        self.dev_io = None if mapped else torch.empty(self.io_bytes, dtype=torch.uint8, device=dev)
         ri, ti, oi = plan.device_arrays(dev)
         self.ws = (torch.empty(max(1, s.num_chunks), s.num_qo_heads, s.head_dim, device=dev),
                    torch.empty(max(1, s.num_chunks), s.num_qo_heads, device=dev))
@@ -637,8 +645,9 @@ class HostStep:
                                                                                            s.head_dim)
         self.lse = self.host_out[16 + rows * s.head_dim * 4:].view(torch.float32).view(s.batch, s.num_qo_heads)
         self._keep = (k_pool, v_pool, ri, ti, oi, stream)
-        self._fn = lib().pa_v2_decode_host
-        self._args = (ctypes.byref(s), self.host_in.data_ptr(), self.host_out.data_ptr(), self.dev_io.data_ptr(),
+        self._fn = lib().pa_v2_decode_host_mapped if mapped else lib().pa_v2_decode_host
+        io = () if mapped else (self.dev_io.data_ptr(),)
+        self._args = (ctypes.byref(s), self.host_in.data_ptr(), self.host_out.data_ptr(), *io,
                       _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"), KV_DTYPES[k_pool.dtype],
                       k_pool.shape[0], ri.data_ptr(), ti.data_ptr(), oi.data_ptr())
         self._tail = (self.ws[0].data_ptr(), self.ws[1].data_ptr(), _stream(stream))
@@ -646,10 +655,11 @@ class HostStep:
         self._graph_scale = None
         if graph_scale is not None:
             g = ctypes.c_void_p()
-            rc = lib().pa_v2_host_graph_create(*self._args, float(graph_scale), self.ws[0].data_ptr(),
-                                               self.ws[1].data_ptr(), ctypes.byref(g))
+            name = "pa_v2_host_graph_create_mapped" if mapped else "pa_v2_host_graph_create"
+            rc = getattr(lib(), name)(*self._args, float(graph_scale), self.ws[0].data_ptr(), self.ws[1].data_ptr(),
+                                      ctypes.byref(g))
             if rc != PA_OK:
-                raise PaError(rc, "pa_v2_host_graph_create")
+                raise PaError(rc, name)
             self._graph, self._graph_scale = g, float(graph_scale)
             self._lib = lib()
 
@@ -676,7 +686,7 @@ class HostStep:
             return self.out, self.lse
         rc = self._fn(*self._args, float(sm_scale), *self._tail)
         if rc != PA_OK:
-            raise PaError(rc, "pa_v2_decode_host")
+            raise PaError(rc, "pa_v2_decode_host_mapped" if self.mapped else "pa_v2_decode_host")
         return self.out, self.lse
 
 

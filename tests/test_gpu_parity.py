@@ -6,6 +6,7 @@ dims, GQA ratios, dtypes and page sizes with ragged lengths, mid-page window
 starts and empty requests, chunk-size invariance, the merge kernel alone, and
 the cascade composition.
 """
+import ctypes
 import math
 import random
 import zlib
@@ -458,7 +459,8 @@ def test_autotune_times_candidates_and_tuned_plan_is_exact(fused):
 
 @pytest.mark.parametrize("name", ["tiny_csr", "sliding_window_batch", "nomerge"])
 @pytest.mark.parametrize("graph", [False, True])
-def test_host_step_matches_the_device_path(name, graph):
+@pytest.mark.parametrize("mapped", [False, True])
+def test_host_step_matches_the_device_path(name, graph, mapped):
     if name == "nomerge":
         b = W.make_batch("nomerge", [40, 17, 0], [0, 3, 0], 16, 8, 2, 128, torch.float16, seed=23)
         plan = make_plan(b, target=1)
@@ -467,9 +469,9 @@ def test_host_step_matches_the_device_path(name, graph):
         b = W.WORKLOADS[name]()
         plan = make_plan(b)
     d = b.to("cuda")
-    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None)
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None, mapped=mapped)
     step.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
-    for _ in range(2):                                  # the status slot is re-zeroed by every copy
+    for _ in range(2):                                  # the status slot is re-zeroed by every step
         o, l = step.run(b.scale)
     ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
                                     b.first_page_offset, b.scale)
@@ -480,11 +482,12 @@ def test_host_step_matches_the_device_path(name, graph):
 
 
 @pytest.mark.parametrize("graph", [False, True])
-def test_host_step_refuses_a_stale_plan_and_reports_bad_pages(graph):
+@pytest.mark.parametrize("mapped", [False, True])
+def test_host_step_refuses_a_stale_plan_and_reports_bad_pages(graph, mapped):
     b = W.make_batch("hs", [100, 60], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
     plan = make_plan(b, target=16)
     d = b.to("cuda")
-    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None)
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b.scale if graph else None, mapped=mapped)
     grown = W.make_batch("hs", [100, 90], [0, 0], 16, 8, 2, 128, torch.float16, seed=24)
     step.pack(grown.q, grown.indices[:b.indices.numel()], grown.indptr, grown.last_page_len,
               grown.first_page_offset)
@@ -504,13 +507,15 @@ def test_host_step_refuses_a_stale_plan_and_reports_bad_pages(graph):
     assert_close(o.clone(), l.clone(), ref_o, ref_l, "host step after errors")
 
 
-def test_host_graph_replays_new_inputs_and_other_scales_take_the_direct_path():
-    """The graph binds buffers and scale; each run reads the step's current host inputs."""
+@pytest.mark.parametrize("mapped", [False, True])
+def test_host_graph_replays_new_inputs_and_other_scales_take_the_direct_path(mapped):
+    """The graph binds buffers and scale; each run reads the step's current host inputs (mapped: the kernels
+    read them from host memory, written by the host between steps)."""
     sets = [W.make_batch("hg", [300, 200], [0, 5], 16, 8, 2, 128, torch.float16, seed=s) for s in (31, 32)]
     b0 = sets[0]
     plan = make_plan(b0, target=32)
     d = b0.to("cuda")
-    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b0.scale)
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b0.scale, mapped=mapped)
     for b in sets:  # same geometry and pool; new q and a new page permutation of the same pool
         q = b.q
         step.pack(q, b0.indices.flip(0).contiguous(), b0.indptr, b0.last_page_len, b0.first_page_offset)
@@ -519,3 +524,30 @@ def test_host_graph_replays_new_inputs_and_other_scales_take_the_direct_path():
             ref_o, ref_l = oracle.attention(q, b0.k_pool, b0.v_pool, b0.indices.flip(0).contiguous(), b0.indptr,
                                             b0.last_page_len, b0.first_page_offset, scale)
             assert_close(o.clone(), l.clone(), ref_o, ref_l, f"host graph scale {scale}")
+
+
+def test_mapped_host_step_refuses_unaligned_buffers():
+    """The copy-free calls need 16-byte aligned host buffers; an unaligned one is refused before any launch."""
+    b = W.make_batch("hm", [40, 17], [0, 3], 16, 8, 2, 128, torch.float16, seed=25)
+    plan = make_plan(b, target=8)
+    d = b.to("cuda")
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, mapped=True)
+    step.pack(b.q, b.indices, b.indptr, b.last_page_len, b.first_page_offset)
+    ri, ti, oi = plan.device_arrays(d.q.device)
+    ws_v, ws_l = step.ws
+    big = torch.zeros(step.in_bytes + 16, dtype=torch.uint8).pin_memory()
+    big[4:4 + step.in_bytes] = step.host_in          # the same words, 4 bytes off a 16-byte boundary
+    L = pa.lib()
+    args = (d.k_pool.data_ptr(), d.v_pool.data_ptr(), pa.KV_DTYPES[d.k_pool.dtype], d.k_pool.shape[0],
+            ri.data_ptr(), ti.data_ptr(), oi.data_ptr(), float(b.scale), ws_v.data_ptr(), ws_l.data_ptr())
+    stream = torch.cuda.current_stream().cuda_stream
+    assert L.pa_v2_decode_host_mapped(ctypes.byref(plan.struct), big.data_ptr() + 4, step.host_out.data_ptr(),
+                                      *args, stream) == pa.PA_EINVAL
+    g = ctypes.c_void_p()
+    assert L.pa_v2_host_graph_create_mapped(ctypes.byref(plan.struct), step.host_in.data_ptr(),
+                                            step.host_out.data_ptr() + 4, *args, ctypes.byref(g)) == pa.PA_EINVAL
+    assert not g.value
+    o, l = step.run(b.scale)                          # the aligned buffers still work
+    ref_o, ref_l = oracle.attention(b.q, b.k_pool, b.v_pool, b.indices, b.indptr, b.last_page_len,
+                                    b.first_page_offset, b.scale)
+    assert_close(o.clone(), l.clone(), ref_o, ref_l, "mapped host step")
