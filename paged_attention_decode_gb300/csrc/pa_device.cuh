@@ -66,6 +66,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Prefetch the 128-byte line holding `a` (global memory) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
+}
+
 // L2 policy for data read exactly once (K/V pages): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -23,6 +23,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "pa_launch.h"
 #include "pa_v2.h"
 
 namespace {
@@ -110,14 +111,15 @@ pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void*
 
   pa_status rc;
   if (plan->needs_merge) {
-    rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
-                              fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse, status, cs);
+    rc = pa::decode_partial_leading(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr,
+                                    lpl, fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse,
+                                    status, cs);
     if (rc == PA_OK)
       rc = pa_merge_states(workspace_v, workspace_lse, o_indptr, B, plan->num_chunks, plan->num_qo_heads,
                            plan->head_dim, out, lse, status, cs);
   } else {
-    rc = pa_v2_decode_partial(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr, lpl,
-                              fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cs);
+    rc = pa::decode_partial_leading(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr,
+                                    lpl, fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cs);
   }
   if (rc != PA_OK) return rc;
   if (!mapped &&

@@ -63,6 +63,7 @@ struct PartialParams {
   uint32_t ps_magic;   // fast division by page_size (see FastDiv)
   uint32_t ps_shift;
   float scale_log2;    // sm_scale * log2(e)
+  int32_t warm_l2;     // prefetch each warp's first stage into L2 before waiting for the kernel before
 };
 
 // Division of a non-negative 32-bit n by a fixed divisor d >= 1 with one
@@ -142,7 +143,16 @@ struct StageGeom {
 // Chunk c covers page slots [tile * ppc, min((tile + 1) * ppc, pages)) of its
 // request; the kernel walks those slots directly.  A stage is 16 pool rows:
 // floor(16 / ps) whole pages when ps <= 16, else one 16-row slice of a page.
+//
+// SPEC: a speculative read, made before the kernel has waited for the one
+// before it, which may still be writing these arrays.  Loads go through L2 only
+// (ld.global.cg: no L1 copy that could outlive the wait), every value is
+// checked before it is used as an index, nothing is reported, and the result
+// only ever chooses prefetch addresses (bad is set and n_stages is 0 when a
+// value is out of range).
+template <bool SPEC = false>
 __device__ __forceinline__ ChunkGeom chunk_geom(const PartialParams& p, int c, int* r_out) {
+  auto ld = [](const int32_t* a) -> int32_t { return SPEC ? __ldcg(a) : *a; };
   ChunkGeom g;
   int r = 0, tile = c;
   bool bad = false;
@@ -152,23 +162,24 @@ __device__ __forceinline__ ChunkGeom chunk_geom(const PartialParams& p, int c, i
     g.slot_base = 0;
     g.pages = p.single_pages;
   } else {
-    r = p.request_indices[c];
-    tile = p.kv_tile_indices[c];
+    r = ld(p.request_indices + c);
+    tile = ld(p.kv_tile_indices + c);
     if (r < 0 || r >= p.batch) {
-      if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_REQUEST);
+      if (!SPEC && threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_REQUEST);
       bad = true;
       r = 0;
     }
-    g.slot_base = p.indptr[r];
-    g.pages = p.indptr[r + 1] - g.slot_base;
+    g.slot_base = ld(p.indptr + r);
+    g.pages = ld(p.indptr + r + 1) - g.slot_base;
     if (!bad && (g.slot_base < 0 || g.pages < 0 || (int64_t)g.slot_base + g.pages > p.num_indices)) {
-      if (threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_SLOT);
+      if (!SPEC && threadIdx.x == 0) report(p.status, PA_DEVICE_BAD_SLOT);
       bad = true;
     }
+    if (SPEC && (tile < 0 || (int64_t)tile * p.pages_per_chunk >= g.pages)) bad = true;
   }
-  g.fpo = p.first_page_offset[r];
-  g.lpl = p.last_page_len[r];
-  g.s_begin = tile * p.pages_per_chunk;
+  g.fpo = SPEC ? 0 : p.first_page_offset[r];
+  g.lpl = SPEC ? p.page_size : p.last_page_len[r];
+  g.s_begin = bad && SPEC ? 0 : tile * p.pages_per_chunk;
   g.s_end = min(g.s_begin + p.pages_per_chunk, g.pages);
   const int ps = p.page_size;
   if (bad || g.s_end <= g.s_begin) {

@@ -80,6 +80,40 @@ __device__ __forceinline__ void partial_tc_body(const CUtensorMap& tm_k, const C
   // it waits for this grid to finish
   pdl_launch_dependents();
 
+  // Before the wait, while the kernel before this one may still be running
+  // (its last CTAs, or the merge of the step before): warm L2 with this warp's
+  // first stage, from a speculative read of the chunk geometry and of the
+  // stage's page ids.  Nothing read here reaches the result -- values are
+  // bounds-checked and only choose prefetch addresses -- and all of it is read
+  // again after the wait; the stage's loads then find their rows in L2 instead
+  // of waiting out a DRAM round trip behind the page-id load.  Lines are
+  // prefetched from the load/store path, leaving the TMA unit to the stages'
+  // loads.  One stage, not the ring's NSW: when nothing runs before this
+  // kernel the prefetches are still in flight as the stages' own loads go out,
+  // and prefetching NSW stages cost such a launch 2-4 us on GB300.  The host
+  // sets warm_l2 where the chain ahead of the prefetches is short (see
+  // prepare_decode).
+  if (p.warm_l2) {
+    int rs;
+    const ChunkGeom sg = chunk_geom<true>(p, c, &rs);
+    if (warp < sg.n_stages) {  // warp-uniform
+      const StageGeom st = stage_geom(sg, warp, ps);
+      const int tp = lane & 15;  // row (tp) of the stage; K for lanes 0-15, V for 16-31
+      const int32_t pg = tp < st.npages ? __ldcg(p.indices + sg.slot_base + st.slot + tp) : -1;
+      const int sl = (int)fast_div((uint32_t)tp, p.ps_magic, p.ps_shift);  // page of row tp within the stage
+      const int32_t page = __shfl_sync(0xffffffffu, pg, sl & 15);
+      const int rows = ps <= kStageRows ? st.npages * ps : kStageRows;
+      if (tp < rows && page >= 0 && (int64_t)page < p.num_pages) {
+        constexpr int ROW_BYTES = D * (int)sizeof(T);
+        const unsigned char* pool = static_cast<const unsigned char*>(lane >= 16 ? p.v_pool : p.k_pool);
+        const unsigned char* a =
+            pool + (((size_t)page * ps + st.row0 + (tp - sl * ps)) * p.num_kv_heads + kvh) * ROW_BYTES;
+#pragma unroll
+        for (int b = 0; b < ROW_BYTES; b += 128) prefetch_l2(a + b);
+      }
+    }
+  }
+
   // launched as a programmatic dependent: the kernel before this one in the
   // stream has completed, and its writes are visible, once this returns
   pdl_wait_prerequisites();
