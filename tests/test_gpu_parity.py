@@ -291,6 +291,24 @@ def test_sweep_ragged(dt, D, G, ps):
     check_batch(b, target=rnd.choice([1, 64, 700]), override=rnd.choice([0, 0, 1, 3]))
 
 
+ONE_REQUEST = [(dt, D, ps) for dt in (torch.float16, torch.bfloat16) for D in (64, 128)
+               for ps in (1, 4, 5, 8, 16, 32, 64, 256)]
+
+
+@pytest.mark.parametrize("dt,D,ps", ONE_REQUEST)
+def test_sweep_one_request(dt, D, ps):
+    """One-request plans (the kernel's single-request geometry and its pre-wait L2 warm-up) on every
+    staging path: cp.async for page sizes 1-5, TMA for 8, 16 and the multiples of 16; a window that
+    starts mid-page and a ragged last page; several chunks."""
+    rnd = random.Random(zlib.crc32(repr(("one", str(dt), D, ps)).encode()))
+    G = rnd.choice([1, 2, 4, 8, 16])
+    L = rnd.randint(40 * max(ps, 8), 60 * max(ps, 8))
+    b = W.make_batch("one", [L], [rnd.randrange(ps)], ps, num_qo_heads=2 * G, num_kv_heads=2, head_dim=D,
+                     dtype=dt, seed=rnd.randint(0, 10 ** 6), order="shuffled")
+    plan, _, _, _ = check_batch(b, target=rnd.choice([64, 152, 700]), override=rnd.choice([0, 0, 3]))
+    assert plan.batch == 1 and plan.num_chunks > 1
+
+
 def test_chunk_size_invariance_seven_sizes():
     b = W.make_batch("inv", [4099, 77, 1, 2500], [5, 0, 0, 15], 16, 32, 8, 128, torch.float16, seed=5)
     outs = []
