@@ -973,7 +973,8 @@ def measure_workload(args):
             "arms": res, "pct_of_hbm_peak": 100.0 * main["kv_read_gbs"] / peak, "hbm_peak_gbs": peak,
             "steady": steady, "oracle_check": oracle_check}
     if cascade:
-        line["config"]["cascade"] = {"pages_per_chunk": cplan.level0.pages_per_chunk,
+        line["config"]["cascade"] = {"level0_pages_per_chunk": cplan.level0.pages_per_chunk,
+                                     "level1_pages_per_chunk": cplan.level1.pages_per_chunk,
                                      "level0_chunks": cplan.level0.num_chunks, "level1_chunks": cplan.level1.num_chunks,
                                      "ctas": cplan.level0.total_ctas + cplan.level1.total_ctas,
                                      "merge_rows": cplan.plans.merge_rows}

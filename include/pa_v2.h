@@ -34,8 +34,12 @@
  *    (passed as void*; NULL is the legacy default stream).  Every kernel is
  *    launched with programmatic stream serialization: it may become resident
  *    while the kernel before it in the stream is finishing, but it waits for
- *    that kernel to complete (griddepcontrol.wait) before its first
- *    global-memory access, so stream order is kept for every buffer.  Each
+ *    that kernel to complete (griddepcontrol.wait) before any global-memory
+ *    access that reaches its results, so stream order is kept for every
+ *    buffer.  (Before that wait, the partial kernels of a one-request plan
+ *    read their first page ids through L2 and prefetch those K/V rows into
+ *    L2: speculative reads, range-checked, never written and never used for
+ *    a result, which is computed from what is read after the wait.)  Each
  *    kernel also lets the one after it be scheduled early, at its own start.
  *  - Units.  Every LSE is in log2 units (scores run in base 2 with log2(e)
  *    folded into the scale); the natural-log LSE is lse2 * ln 2.
@@ -290,10 +294,14 @@ pa_status pa_v2_cascade_split(const int32_t* indptr, const int32_t* indices, con
  *    l1_first_page_offset, l1_seq_lens or null; l1_batch requests, host
  *    arrays as for pa_v2_plan).  member_requests[m] (host, or null for m) is
  *    member m's request in that table.
- * Both levels take ONE chunk size, the smallest whose CTAs -- one chunk's
+ * Chunk sizes: first the common size, the smallest whose CTAs -- one chunk's
  * CTAs (num_kv_heads x q-groups of the level) per chunk, summed over both
- * levels -- fit `wave_ctas`, so every CTA of the launch reads at most as many
- * pages as any other (the longest request's size when none fits).  Each plan
+ * levels -- fit `wave_ctas` (the longest request's size when none fits);
+ * level 1 takes it.  Level 0, whose chunks carry the stacked heads of every
+ * member, takes the CTAs left over: the smallest size whose chunks fit
+ * `wave_ctas` beside level 1's (at most the common size; when nothing fits,
+ * the common size).  No CTA of the launch reads more pages than the common
+ * size.  Each plan
  * is written as pa_v2_plan writes it (arrays into the l0_ / l1_ buffers;
  * level 0 has one request, so l0_o_indptr holds 2 entries), plan0 with
  * stack_members = members.  The merge input puts request r's rows together:

@@ -18,10 +18,12 @@ library, both from one C call (``pa_v2_cascade_decode``):
    folding a request's chunks of both levels at once is the cascade's
    two-state merge).
 
-``pa_v2_cascade_plan`` gives both levels one chunk size, the smallest whose
-CTAs fit one wave, so the two levels run side by side and no CTA reads more
-than another.  For a flat batch, ``pa_v2_cascade_detect`` finds the shared prefix
-and ``pa_v2_cascade_split`` builds the level-1 table and the row maps.
+``pa_v2_cascade_plan`` sizes the chunks so both levels fit one wave and run
+side by side: level 1 at the smallest common size whose CTAs over both levels
+fit, level 0 (whose chunks carry every member's stacked heads) at the smallest
+size that uses the CTAs left over.  For a flat batch, ``pa_v2_cascade_detect``
+finds the shared prefix and ``pa_v2_cascade_split`` builds the level-1 table
+and the row maps.
 
 This module only builds plans and marshals buffers; every step runs in the
 library's kernels.
@@ -81,7 +83,7 @@ def _wave(num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype):
 def cascade_plan(shared_pages: int, suffix_indptr, suffix_last_page_len, suffix_first_page_offset,
                  page_size: int, num_qo_heads: int, num_kv_heads: int, head_dim: int, kv_dtype: int,
                  wave_ctas: int = 0, suffix_seq_lens=None) -> CascadePlan:
-    """Plans for both levels (pa_v2_cascade_plan: one chunk size whose CTAs fit one wave of `wave_ctas`, 0 =
+    """Plans for both levels (pa_v2_cascade_plan: chunk sizes whose CTAs fit one wave of `wave_ctas`, 0 =
     the device's).  The shared span is `shared_pages` full pages; the suffix table is host data."""
     M = len(suffix_indptr) - 1
     wave = wave_ctas or _wave(num_qo_heads, num_kv_heads, head_dim, page_size, kv_dtype)

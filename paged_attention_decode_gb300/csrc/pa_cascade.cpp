@@ -161,7 +161,7 @@ extern "C" pa_status pa_v2_cascade_plan(int32_t members, int32_t shared_pages, c
     if (pages1[r] < 0) return PA_EGEOMETRY;
     longest = std::max(longest, pages1[r]);
   }
-  // one chunk size for both levels: the smallest whose CTAs (non-increasing in the size) fit the wave
+  // a common chunk size for both levels: the smallest whose CTAs (non-increasing in the size) fit the wave
   auto ctas = [&](int64_t size) {
     int64_t n = per0 * ((shared_pages + size - 1) / size);
     for (int64_t p : pages1) n += per1 * (p > size ? (p + size - 1) / size : 1);
@@ -177,12 +177,22 @@ extern "C" pa_status pa_v2_cascade_plan(int32_t members, int32_t shared_pages, c
     }
   }
   const int32_t ppc = static_cast<int32_t>(lo);
+  // Level 0 then takes the CTAs that size leaves idle: its chunks carry the members' stacked query heads
+  // (members x G per KV head against level 1's G), so its pages cost the most; its size is the smallest
+  // whose chunks fit the wave beside level 1's chunks at the common size (it only shrinks).
+  int32_t ppc0 = ppc;
+  if (ctas(lo) <= wave_ctas) {
+    int64_t n1 = 0;
+    for (int64_t p : pages1) n1 += per1 * (p > lo ? (p + lo - 1) / lo : 1);
+    const int64_t chunks0 = std::min<int64_t>((wave_ctas - n1) / per0, PA_V2_MAX_CHUNKS);  // >= ceil(shared / lo)
+    ppc0 = static_cast<int32_t>((shared_pages + chunks0 - 1) / chunks0);
+  }
 
   const int32_t ip0[2] = {0, shared_pages};
   const int32_t lp0[1] = {page_size};
   const int32_t fp0[1] = {0};
   pa_status rc = pa_v2_plan(ip0, lp0, fp0, nullptr, 1, page_size, members * num_qo_heads, num_kv_heads, head_dim,
-                            kv_dtype, wave_ctas, ppc, l0_request_indices, l0_kv_tile_indices, l0_cap_chunks,
+                            kv_dtype, wave_ctas, ppc0, l0_request_indices, l0_kv_tile_indices, l0_cap_chunks,
                             l0_o_indptr, plan0);
   if (rc != PA_OK) return rc;
   plan0->stack_members = members;

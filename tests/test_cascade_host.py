@@ -116,24 +116,26 @@ def test_split_rebuilds_the_flat_tables():
 
 def test_cascade_plan_by_hand():
     # 4 members share 512 pages; suffixes of 25, 94, 62 and 91 pages; one wave of 152 CTAs, 8 CTAs per chunk at
-    # either level (Hkv 8, one q-group).  One chunk size for both levels: 47 pages make 11 + (1 + 2 + 2 + 2) = 18
-    # chunks = 144 CTAs; 46 pages would make 12 + (1 + 3 + 2 + 2) = 20 = 160
+    # either level (Hkv 8, one q-group).  The common size: 47 pages make 11 + (1 + 2 + 2 + 2) = 18 chunks = 144
+    # CTAs; 46 pages would make 12 + (1 + 3 + 2 + 2) = 20 = 160.  Level 1 keeps 47 (7 chunks, 56 CTAs); level 0
+    # takes the other 96 CTAs: 12 chunks, ceil(512 / 12) = 43 pages (11 x 43 + 39)
     c = pa.pa_v2_cascade_plan(4, 512, [0, 25, 119, 181, 272], [16, 4, 7, 16], [0, 0, 0, 0], 16, 32, 8, 128,
                               pa.PA_F16, 152)
-    assert (c.level0.pages_per_chunk, c.level0.num_chunks, c.level1.num_chunks) == (47, 11, 7)
-    assert c.level1.pages_per_chunk == 47 and c.level0.total_ctas + c.level1.total_ctas == 144
+    assert (c.level0.pages_per_chunk, c.level0.num_chunks, c.level1.num_chunks) == (43, 12, 7)
+    assert c.level1.pages_per_chunk == 47 and c.level0.total_ctas + c.level1.total_ctas == 152
     assert (c.level0.stack_members, c.level0.num_qo_heads, c.level0.batch) == (4, 128, 1)
-    # merge input, request by request: 11 level-0 rows then the request's level-1 rows
-    assert c.merge_indptr.tolist() == [0, 12, 25, 38, 51]
-    assert c.l0_part_rows.tolist() == [0, 12, 25, 38]
+    # merge input, request by request: 12 level-0 rows then the request's level-1 rows
+    assert c.merge_indptr.tolist() == [0, 13, 27, 41, 55]
+    assert c.l0_part_rows.tolist() == [0, 13, 27, 41]
     # level-1 chunk j of request r lands at l1_part_rows[r] + j: chunks 0 | 1, 2 | 3, 4 | 5, 6
-    assert c.l1_part_rows.tolist() == [11, 22, 33, 44]
+    assert c.l1_part_rows.tolist() == [12, 24, 36, 48]
 
 
 def test_cascade_plan_brute_force():
-    """The chunk size and the merge layout against their definitions on random batches, members anywhere in
-    the level-1 table: the smallest size whose CTAs over both levels fit the wave; each request's rows are its
-    level-0 chunks (members) then its level-1 chunks; every row is written exactly once."""
+    """The chunk sizes and the merge layout against their definitions on random batches, members anywhere in
+    the level-1 table: level 1 at the smallest common size whose CTAs over both levels fit the wave, level 0 at
+    the smallest size whose chunks fit beside level 1's; each request's rows are its level-0 chunks (members)
+    then its level-1 chunks; every row is written exactly once."""
     rng = random.Random(11)
     for _ in range(300):
         B = rng.randint(1, 7)
@@ -156,7 +158,14 @@ def test_cascade_plan_brute_force():
             return per0 * -(-shared // k) + per1 * sum(max(1, -(-p // k)) for p in pages)
         fits = [k for k in range(1, max(pages + [shared]) + 1) if ctas(k) <= wave]
         want = min(fits) if fits else max(pages + [shared])
-        assert c.level0.pages_per_chunk == c.level1.pages_per_chunk == want
+        assert c.level1.pages_per_chunk == want
+        want0 = want
+        if fits:
+            ctas1 = per1 * sum(max(1, -(-p // want)) for p in pages)
+            want0 = min(k for k in range(1, want + 1) if per0 * -(-shared // k) + ctas1 <= wave)
+            assert c.level0.total_ctas + c.level1.total_ctas <= wave
+        assert c.level0.pages_per_chunk == want0, (want0, c.level0.pages_per_chunk)
+        assert c.level0.num_chunks == -(-shared // want0)
         n0 = c.level0.num_chunks
         o1 = c.level1.o_indptr.tolist()
         rows = []
