@@ -532,13 +532,21 @@ void pa_v2_host_graph_destroy(pa_v2_host_graph_t* graph);
  * partial kernel reads q and the page table from host_in through its device
  * address, and the last kernel writes out and lse2 into host_out, whose first
  * 16 bytes are the status slot: the call (or run()) zeroes it from the host
- * before the launch, and the kernels OR their error bits into it.  host_in's
- * trailing status slot is not used, and there is no dev_io.
+ * before the launch, and the kernels OR their error bits into word 0.  When
+ * the plan merges, each merge CTA adds one to word 1 once its results are
+ * visible to the host (a system-scope fence first), and the call returns as
+ * soon as that count is complete rather than after synchronising cuda_stream
+ * (after ~5 s without it, it synchronises): the step's kernels may still be
+ * retiring when it returns.  Work queued on cuda_stream afterwards is ordered
+ * after them; synchronise the stream before freeing either buffer or handing
+ * it to another stream.  host_in's trailing status slot is not used, and
+ * there is no dev_io.
  *
  * pa_v2_decode_host_mapped: check the plan against host_in's page table
  * (PA_EGEOMETRY, nothing launched), launch the partial kernel and the merge
- * when plan->needs_merge, synchronize cuda_stream and return
- * pa_status_from_device of the status word.  PA_EINVAL as pa_v2_decode_host,
+ * when plan->needs_merge, wait for the merge's count (or, without a merge,
+ * synchronize cuda_stream) and return pa_status_from_device of the status
+ * word.  PA_EINVAL as pa_v2_decode_host,
  * and when host_in or host_out is unaligned or has no device mapping.
  *
  * pa_v2_host_graph_create_mapped: capture the same two launches as a graph,

@@ -17,9 +17,13 @@
 // last kernel writes the status, out and lse2 straight into host_out: each step
 // is then two kernel launches, the second a programmatic dependent of the first,
 // instead of copy -> partial -> merge -> copy with a full dependency at either
-// copy.
+// copy.  The merge also counts its finished CTAs into the status slot, and the
+// host waits for that count instead of synchronising the stream: the results
+// are in host memory before the launch has formally completed.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 
@@ -63,12 +67,15 @@ unsigned char* mapped_address(const void* host) {
 // arguments and the plan against the step's page table first.  With `mapped`
 // (the device addresses of host_in and host_out, from mapped_address): no
 // copies; the kernels read and write those, the status word is host_out's,
-// which the caller zeroes before the step, and dev_io is not used.
+// which the caller zeroes before the step, dev_io is not used, and the merge
+// counts its finished CTAs into the slot's second word (*merge_ctas of them; 0
+// when the step has no merge and the caller must synchronise instead).
 pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
                             const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
                             const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
                             float sm_scale, float* workspace_v, float* workspace_lse, cudaStream_t stream,
-                            bool check_geometry, unsigned char* const* mapped) {
+                            bool check_geometry, unsigned char* const* mapped, int64_t* merge_ctas) {
+  *merge_ctas = 0;
   int64_t in_bytes = 0, out_bytes = 0, io_bytes = 0;
   if (pa_v2_host_io_layout(plan, &in_bytes, &out_bytes, &io_bytes) != PA_OK) return PA_EINVAL;
   if (!host_in || !host_out) return PA_EINVAL;
@@ -115,8 +122,9 @@ pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void*
                                     lpl, fpo, request_indices, kv_tile_indices, sm_scale, workspace_v, workspace_lse,
                                     status, cs);
     if (rc == PA_OK)
-      rc = pa_merge_states(workspace_v, workspace_lse, o_indptr, B, plan->num_chunks, plan->num_qo_heads,
-                           plan->head_dim, out, lse, status, cs);
+      rc = pa::launch_merge(workspace_v, workspace_lse, o_indptr, B, plan->num_chunks, plan->num_qo_heads,
+                            plan->head_dim, out, lse, status, mapped ? status + 1 : nullptr,
+                            mapped ? merge_ctas : nullptr, cs);
   } else {
     rc = pa::decode_partial_leading(plan, q, k_pool, v_pool, kv_dtype, num_pages, indices, plan->num_indices, indptr,
                                     lpl, fpo, request_indices, kv_tile_indices, sm_scale, out, lse, status, cs);
@@ -130,6 +138,34 @@ pa_status enqueue_host_step(const pa_v2_plan_t* plan, const void* host_in, void*
 
 void clear_status_slot(void* host_out) { std::memset(host_out, 0, 16); }
 
+// Wait for the merge's count of finished CTAs in host_out's status slot to reach
+// `ctas` (each CTA adds one after a system-scope fence behind its stores), then
+// order the reads that follow after it.  False after ~5 s without it.
+bool wait_merge_count(const void* host_out, int64_t ctas) {
+  const volatile int32_t* count =
+      reinterpret_cast<const volatile int32_t*>(static_cast<const unsigned char*>(host_out) + 4);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (uint32_t i = 1;; ++i) {
+    if (*count >= ctas) {
+      std::atomic_thread_fence(std::memory_order_acquire);
+      return true;
+    }
+    if ((i & 4095u) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::seconds(5)) return false;
+  }
+}
+
+// The end of a host step: wait for the merge's count when there is one (the
+// stream is then left to retire the step's kernels on its own), else, or when
+// the count never comes, synchronise the stream; then the status word.
+pa_status finish_host_step(cudaStream_t stream, const void* host_out, int64_t merge_ctas) {
+  if (merge_ctas <= 0 || !wait_merge_count(host_out, merge_ctas)) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
+  }
+  int32_t word = 0;
+  std::memcpy(&word, host_out, sizeof(word));
+  return pa_status_from_device(word);
+}
+
 pa_status decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_out, void* dev_io,
                       const void* k_pool, const void* v_pool, int32_t kv_dtype, int64_t num_pages,
                       const int32_t* request_indices, const int32_t* kv_tile_indices, const int32_t* o_indptr,
@@ -141,17 +177,15 @@ pa_status decode_host(const pa_v2_plan_t* plan, const void* host_in, void* host_
     addr[1] = mapped_address(host_out);
     if (addr[1]) clear_status_slot(host_out);
   }
+  int64_t merge_ctas = 0;
   const pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
                                          request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v,
-                                         workspace_lse, stream, true, mapped ? addr : nullptr);
+                                         workspace_lse, stream, true, mapped ? addr : nullptr, &merge_ctas);
   if (rc != PA_OK) {
     cudaStreamSynchronize(stream);  // a copy or kernel already queued may still be reading host_in
     return rc;
   }
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
-  int32_t word = 0;
-  std::memcpy(&word, host_out, sizeof(word));
-  return pa_status_from_device(word);
+  return finish_host_step(stream, host_out, merge_ctas);
 }
 
 }  // namespace
@@ -188,7 +222,8 @@ struct pa_v2_host_graph {
   pa_v2_plan_t plan;
   const void* host_in;
   void* host_out;
-  bool mapped;  // the status slot is host_out's, zeroed by run()
+  bool mapped;         // the status slot is host_out's, zeroed by run()
+  int64_t merge_ctas;  // mapped: the merge CTAs run() waits to see counted (0: synchronise)
   cudaGraph_t graph;
   cudaGraphExec_t exec;
 };
@@ -216,9 +251,10 @@ pa_status host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void*
     return PA_ECUDA;
   }
   // the geometry is checked on every run, against that step's page table
+  int64_t merge_ctas = 0;
   pa_status rc = enqueue_host_step(plan, host_in, host_out, dev_io, k_pool, v_pool, kv_dtype, num_pages,
                                    request_indices, kv_tile_indices, o_indptr, sm_scale, workspace_v, workspace_lse,
-                                   cap, false, mapped ? addr : nullptr);
+                                   cap, false, mapped ? addr : nullptr, &merge_ctas);
   cudaGraph_t graph = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
   cudaStreamDestroy(cap);
@@ -235,6 +271,7 @@ pa_status host_graph_create(const pa_v2_plan_t* plan, const void* host_in, void*
   g->host_in = host_in;
   g->host_out = host_out;
   g->mapped = mapped;
+  g->merge_ctas = merge_ctas;
   g->graph = graph;
   g->exec = exec;
   *out = g;
@@ -275,10 +312,7 @@ extern "C" pa_status pa_v2_host_graph_run(pa_v2_host_graph_t* g, void* cuda_stre
     cudaStreamSynchronize(stream);
     return PA_ECUDA;
   }
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
-  int32_t word = 0;
-  std::memcpy(&word, g->host_out, sizeof(word));
-  return pa_status_from_device(word);
+  return finish_host_step(stream, g->host_out, g->mapped ? g->merge_ctas : 0);
 }
 
 extern "C" void pa_v2_host_graph_destroy(pa_v2_host_graph_t* g) {

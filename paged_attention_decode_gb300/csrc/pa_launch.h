@@ -19,4 +19,14 @@ pa_status decode_partial_leading(const pa_v2_plan_t* plan, const float* q, const
                                  const int32_t* kv_tile_indices, float sm_scale, float* v_out, float* lse2_out,
                                  int32_t* status, void* cuda_stream);
 
+// pa_merge_states with an optional completion count: `done` (or null) is an
+// int32 in memory the host can read -- a word of a mapped host buffer -- to which
+// every CTA adds one after a system-scope fence that follows its stores, so the
+// count reaching *ctas (the CTAs launched; 0 when nothing was) means every result
+// of the merge, and every status bit of the kernels before it, is visible to the
+// host.  Same checks and errors as pa_merge_states.
+pa_status launch_merge(const float* v_in, const float* lse2_in, const int32_t* o_indptr, int32_t num_rows_out,
+                       int32_t num_partials, int32_t num_heads, int32_t head_dim, float* v_out, float* lse2_out,
+                       int32_t* status, int32_t* done, int64_t* ctas, void* cuda_stream);
+
 }  // namespace pa

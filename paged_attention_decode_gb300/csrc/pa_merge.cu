@@ -24,6 +24,7 @@
 #include <cstdint>
 
 #include "pa_device.cuh"
+#include "pa_launch.h"
 #include "pa_v2.h"
 
 namespace pa {
@@ -39,11 +40,11 @@ __device__ __forceinline__ float merge_weight(float l, float m) {
 // NV > 0: head_dim % 4 == 0 and head_dim <= 128 * NV (NV float4 per lane:
 // 1 up to head_dim 128, 4 up to 512); NV == 0: a scalar loop over head_dim.
 template <int NV>
-__global__ void __launch_bounds__(kMergeWarps * 32)
-    pa_merge_states_kernel(const float* __restrict__ v_in, const float* __restrict__ lse_in,
-                           const int32_t* __restrict__ o_indptr, int32_t num_rows_out, int32_t num_partials,
-                           int32_t num_heads, int32_t head_dim, float* __restrict__ v_out,
-                           float* __restrict__ lse_out, int32_t* status) {
+__device__ __forceinline__ void merge_body(const float* __restrict__ v_in, const float* __restrict__ lse_in,
+                                           const int32_t* __restrict__ o_indptr, int32_t num_rows_out,
+                                           int32_t num_partials, int32_t num_heads, int32_t head_dim,
+                                           float* __restrict__ v_out, float* __restrict__ lse_out,
+                                           int32_t* status) {
   __shared__ float red[kMergeWarps];
   __shared__ float wsum_s[kMergeWarps];
   constexpr bool VECTOR = NV > 0;
@@ -176,14 +177,30 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
 }
 
-}  // namespace
-}  // namespace pa
+// done (or null): a counter in memory the host can read; each CTA adds one once
+// its results are visible system-wide, so a host thread can wait for the count
+// instead of synchronising the stream.
+template <int NV>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    pa_merge_states_kernel(const float* __restrict__ v_in, const float* __restrict__ lse_in,
+                           const int32_t* __restrict__ o_indptr, int32_t num_rows_out, int32_t num_partials,
+                           int32_t num_heads, int32_t head_dim, float* __restrict__ v_out,
+                           float* __restrict__ lse_out, int32_t* status, int32_t* done) {
+  merge_body<NV>(v_in, lse_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse_out, status);
+  if (done) {
+    __threadfence_system();  // this thread's results (and status bits) before the count
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd_system(done, 1);
+  }
+}
 
-extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, const int32_t* o_indptr,
-                                     int32_t num_rows_out, int32_t num_partials, int32_t num_heads,
-                                     int32_t head_dim, float* v_out, float* lse2_out, int32_t* status,
-                                     void* cuda_stream) {
+}  // namespace
+
+pa_status launch_merge(const float* v_in, const float* lse2_in, const int32_t* o_indptr, int32_t num_rows_out,
+                       int32_t num_partials, int32_t num_heads, int32_t head_dim, float* v_out, float* lse2_out,
+                       int32_t* status, int32_t* done, int64_t* ctas, void* cuda_stream) {
   if (num_rows_out < 0 || num_partials < 0 || num_heads < 1 || head_dim < 1) return PA_EINVAL;
+  if (ctas) *ctas = 0;
   if (num_rows_out == 0) return PA_OK;
   if (!o_indptr || !v_out || !lse2_out || (num_partials > 0 && (!v_in || !lse2_in))) return PA_EINVAL;
   const int nv = head_dim % 4 != 0 ? 0 : head_dim <= 128 ? 1 : head_dim <= 512 ? 4 : 0;
@@ -196,7 +213,7 @@ extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, co
   // kernel's first instruction waits for that grid to complete.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(pa::kMergeWarps * 32);
+  cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(cuda_stream);
   cudaLaunchAttribute attr[1];
@@ -204,9 +221,20 @@ extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto fn = nv == 1 ? pa::pa_merge_states_kernel<1> : nv == 4 ? pa::pa_merge_states_kernel<4>
-                                                              : pa::pa_merge_states_kernel<0>;
+  auto fn = nv == 1 ? pa_merge_states_kernel<1> : nv == 4 ? pa_merge_states_kernel<4> : pa_merge_states_kernel<0>;
   cudaError_t rc = cudaLaunchKernelEx(&cfg, fn, v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads,
-                                      head_dim, v_out, lse2_out, status);
-  return rc == cudaSuccess && cudaGetLastError() == cudaSuccess ? PA_OK : PA_ECUDA;
+                                      head_dim, v_out, lse2_out, status, done);
+  if (rc != cudaSuccess || cudaGetLastError() != cudaSuccess) return PA_ECUDA;
+  if (ctas) *ctas = blocks;
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_merge_states(const float* v_in, const float* lse2_in, const int32_t* o_indptr,
+                                     int32_t num_rows_out, int32_t num_partials, int32_t num_heads,
+                                     int32_t head_dim, float* v_out, float* lse2_out, int32_t* status,
+                                     void* cuda_stream) {
+  return pa::launch_merge(v_in, lse2_in, o_indptr, num_rows_out, num_partials, num_heads, head_dim, v_out, lse2_out,
+                          status, nullptr, nullptr, cuda_stream);
 }

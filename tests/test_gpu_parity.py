@@ -544,6 +544,32 @@ def test_host_graph_replays_new_inputs_and_other_scales_take_the_direct_path(map
             assert_close(o.clone(), l.clone(), ref_o, ref_l, f"host graph scale {scale}")
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_mapped_host_steps_return_complete_results(graph):
+    """The copy-free calls return once the merge's CTA count in the status slot is complete, before the
+    launch has formally finished: read straight after each of 40 consecutive steps (two input sets in turn,
+    so a step that returned early would still show the other set's results), every output must equal the
+    device path's for that step's inputs, bit for bit."""
+    sets = [W.make_batch("hc", [700, 300, 45], [3, 0, 9], 16, 8, 2, 128, torch.float16, seed=s) for s in (41, 42)]
+    b0 = sets[0]
+    plan = make_plan(b0, target=64)
+    assert plan.needs_merge
+    d = b0.to("cuda")
+    step = pa.HostStep(plan, d.k_pool, d.v_pool, graph_scale=b0.scale if graph else None, mapped=True)
+    tables = [b0.indices, b0.indices.flip(0).contiguous()]
+    want = []
+    for b, tab in zip(sets, tables):
+        o, l = pa.decode(plan, b.q.cuda(), d.k_pool, d.v_pool, tab.cuda(), d.indptr, d.last_page_len,
+                         d.first_page_offset, b0.scale)
+        want.append((o.cpu(), l.cpu()))
+    for i in range(40):
+        b, tab = sets[i % 2], tables[i % 2]
+        step.pack(b.q, tab, b0.indptr, b0.last_page_len, b0.first_page_offset)
+        o, l = step.run(b0.scale)
+        assert torch.equal(o, want[i % 2][0]) and torch.equal(l, want[i % 2][1]), f"step {i}"
+    torch.cuda.synchronize()
+
+
 def test_mapped_host_step_refuses_unaligned_buffers():
     """The copy-free calls need 16-byte aligned host buffers; an unaligned one is refused before any launch."""
     b = W.make_batch("hm", [40, 17], [0, 3], 16, 8, 2, 128, torch.float16, seed=25)
