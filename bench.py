@@ -669,7 +669,7 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
     HostStep on a graph from pa_v2_host_graph_create_mapped -- the cached plan checked against the step's
     page table, the status slot zeroed, one graph launch whose partial kernel reads q and the page table
     from pinned host memory over NVLink-C2C and whose merge writes out and lse2 back into pinned host
-    memory -- and stream synchronisation.  Timed beside it: the same step as one direct
+    memory -- and the wait for the merge's completion count in the status slot.  Timed beside it: the same step as one direct
     pa_v2_decode_host_mapped call, and both again with copy-engine copies (pa_v2_host_graph_create /
     pa_v2_decode_host: one pinned H2D of the packed inputs into a device buffer, one D2H of the outputs).
     The fused one-launch step (--fused) keeps the per-array path: pa_v2_plan_matches, a pinned copy,
@@ -709,8 +709,10 @@ def run_e2e(args, pa, plan, sets_cpu, sets, dev, stream, b0):
             "path": "per step: pa_v2_host_graph_run on a pa_v2_host_graph_create_mapped graph (plan check "
                     "against the step's page table, status slot zeroed, one graph launch: " + STEP_TWO +
                     " with q and the page table read by the partial kernel from pinned host memory over "
-                    "NVLink-C2C and status + out + lse2 written by the merge into pinned host memory; stream "
-                    "sync); direct_call_us_per_step: the same step as one pa_v2_decode_host_mapped call; "
+                    "NVLink-C2C and status + out + lse2 written by the merge into pinned host memory, each merge "
+                    "CTA counting itself into the status slot after a system-scope fence; the host waits for "
+                    "the full count, then reads the results); direct_call_us_per_step: the same step as one "
+                    "pa_v2_decode_host_mapped call; "
                     "copy_engine: the same step with one H2D copy of the packed inputs and one D2H copy of "
                     "the outputs (pa_v2_host_graph_create / pa_v2_decode_host)"}
 
