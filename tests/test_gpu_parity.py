@@ -309,6 +309,19 @@ def test_sweep_one_request(dt, D, ps):
     assert plan.batch == 1 and plan.num_chunks > 1
 
 
+def test_plan_at_the_chunk_cap():
+    """The largest plan the launch shape allows (PA_V2_MAX_CHUNKS = 65535 chunks, the pages' grid bound):
+    21845 requests of three 8-row pages, windows starting and ending mid-page, one page per chunk; merged
+    outputs, fused outputs and every chunk's partial against the oracle."""
+    rnd = random.Random(65535)
+    B = 21845
+    fpos = [rnd.randrange(8) for _ in range(B)]
+    lens = [rnd.randint(17 - f, 24 - f) for f in fpos]     # (fpo + len) in 17..24: exactly three pages
+    b = W.make_batch("cap", lens, fpos, 8, 4, 1, 64, torch.float16, seed=7, slack=1.0)
+    plan, _, _, _ = check_batch(b, target=1, override=1)
+    assert plan.num_chunks == 65535 and plan.needs_merge
+
+
 def test_chunk_size_invariance_seven_sizes():
     b = W.make_batch("inv", [4099, 77, 1, 2500], [5, 0, 0, 15], 16, 32, 8, 128, torch.float16, seed=5)
     outs = []
