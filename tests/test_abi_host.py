@@ -316,3 +316,51 @@ def test_host_graph_rejects_bad_arguments_before_any_cuda_call():
     assert not g.value
     assert L.pa_v2_host_graph_run(None, None) == pa.PA_EINVAL
     L.pa_v2_host_graph_destroy(None)  # a no-op
+
+
+def test_decode_and_merge_reject_bad_arguments_before_any_cuda_call():
+    """Host-side validation of pa_v2_decode_partial / pa_v2_decode / pa_merge_states: every case below returns
+    before a tensor map is encoded or a kernel launched (no device is needed), including the pool-row limit
+    (num_pages * page_size must stay below 2^31) and a plan with no chunks (nothing to launch)."""
+    import ctypes
+    import math
+    L = pa.lib()
+    b = W.make_batch("args", [100, 40], [0, 3], 16, 8, 2, 128, torch.float16, seed=3)
+    plan = pa.pa_v2_plan(b.indptr, b.last_page_len, b.first_page_offset, 16, 8, 2, 128, pa.PA_F16, 16)
+    A = 1 << 20                                     # fake 16-byte-aligned addresses: never dereferenced
+
+    def partial(s=None, q=A, dtype=pa.PA_F16, num_pages=64, num_indices=None, scale=0.1, v_out=A):
+        s = plan.struct if s is None else s
+        n = plan.num_indices if num_indices is None else num_indices
+        return L.pa_v2_decode_partial(ctypes.byref(s) if s is not False else None, q, A, A, dtype, num_pages, A, n,
+                                      A, A, A, A, A, scale, v_out, A, None, None)
+
+    def mutated(**kw):
+        s = pa.PlanStruct.from_buffer_copy(plan.struct)
+        for k, v in kw.items():
+            setattr(s, k, v)
+        return s
+
+    assert partial(s=False) == pa.PA_EINVAL
+    assert partial(q=None) == pa.PA_EINVAL
+    assert partial(q=A + 4) == pa.PA_EINVAL         # misaligned q
+    assert partial(v_out=A + 8) == pa.PA_EINVAL     # misaligned workspace
+    assert partial(dtype=pa.PA_BF16) == pa.PA_EINVAL
+    assert partial(num_pages=0) == pa.PA_EINVAL
+    assert partial(num_indices=plan.num_indices - 1) == pa.PA_EINVAL
+    for bad in (math.inf, math.nan):
+        assert partial(scale=bad) == pa.PA_EINVAL
+    assert partial(num_pages=(1 << 31) // 16) == pa.PA_EUNSUPPORTED      # 2^31 pool rows
+    assert partial(s=mutated(q_heads_per_cta=3)) == pa.PA_EINVAL
+    assert partial(s=mutated(head_dim=96)) == pa.PA_EUNSUPPORTED
+    assert partial(s=mutated(stack_members=0)) == pa.PA_EINVAL
+    assert partial(s=mutated(num_chunks=0)) == pa.PA_OK                 # nothing to launch
+    # the fused entry point: the same checks plus its merge arguments
+    assert L.pa_v2_decode(ctypes.byref(plan.struct), A, A, A, pa.PA_F16, 64, A, plan.num_indices, A, A, A, A, A,
+                          None, 0.1, A, A, A, A, A, None, None, None, None) == pa.PA_EINVAL   # no o_indptr
+    # the merge
+    assert L.pa_merge_states(A, A, A, 2, 5, 0, 128, A, A, None, None) == pa.PA_EINVAL     # no heads
+    assert L.pa_merge_states(A, A, A, -1, 5, 8, 128, A, A, None, None) == pa.PA_EINVAL
+    assert L.pa_merge_states(A + 4, A, A, 2, 5, 8, 128, A, A, None, None) == pa.PA_EINVAL  # misaligned v_in
+    assert L.pa_merge_states(A, A, None, 2, 5, 8, 128, A, A, None, None) == pa.PA_EINVAL   # no o_indptr
+    assert L.pa_merge_states(A, A, A, 0, 5, 8, 128, A, A, None, None) == pa.PA_OK          # no rows: no launch
