@@ -1,20 +1,25 @@
 """The oracle's pins have teeth: plausible mistakes planted in the oracle each fail at least one of them.
 
-Each mutant is the oracle's C source with one edit of the kind a careless restatement of the pages' formulas
-would make (a dropped term, a wrong index or base, an off-by-one, a wrong search rule); it is compiled on the
-CPU, the oracle package is pointed at it, and the pins of ``test_oracle_pins.py`` run until one fails.  The
-unmutated source, compiled the same way, must pass every pin -- so a mutant that survives means a pin is
-missing, not that the runner is broken.  Nothing here touches a GPU.
+Each mutant is the oracle with one edit of the kind a careless restatement of the pages' formulas would make
+(a dropped term, a wrong index or base, an off-by-one, a wrong search or tie rule).  C mutants are compiled on
+the CPU and the oracle package is pointed at the result; Python mutants are a mutated copy of the package's
+source whose edited function replaces the oracle's.  The pins then run until one fails.  The unmutated
+source, through the same runner, must pass every pin -- so a mutant that survives means a pin is missing,
+not that the runner is broken.  Nothing here touches a GPU.
 """
 import inspect
 import itertools
 import os
 import shutil
+import types
 
 import pytest
 
 import oracle
+import test_cascade_host
+import test_extra_pins
 import test_oracle_pins as pins
+import test_selection_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
 
@@ -66,11 +71,52 @@ MUTANTS = [
 ]
 
 
-def _pin_calls():
-    """Every pin of test_oracle_pins as (name, function, kwargs), parametrize marks expanded."""
+OracleSrc = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+# pins only: tests that compare the oracle with the library's own host code are parity checks, not pins
+SELECTION = (test_selection_pins,)
+DETECTION = ((test_cascade_host, {"test_detect_rules_by_hand", "test_detect_tie_goes_to_the_group_met_first"}),
+             pins)
+
+# (what the mistake is, the oracle functions it changes, the exact source text, the replacement, the pin
+# modules to run)
+PY_MUTANTS = [
+    ("detection: on a tie the later group wins", ("cascade_detect_ref",),
+     "        if score > best_score:", "        if score >= best_score:", DETECTION),
+    ("detection: the shared span may cover a member's last page", ("cascade_detect_ref",),
+     "cap = min(ip[r + 1] - ip[r] - 1 for r in mem)", "cap = min(ip[r + 1] - ip[r] for r in mem)", DETECTION),
+    ("detection: windows that start mid-page join a group", ("cascade_detect_ref",),
+     "if fp[r] != 0 or pages < 2:", "if pages < 2:", DETECTION),
+    ("selection: rows one past each block", ("selection_rows_ref",),
+     "out.append(base + j * block_size + e)", "out.append(base + j * block_size + e + 1)", SELECTION),
+    ("selection: request stride ignored", ("selection_rows_ref",),
+     "        base = r * request_stride\n", "        base = 0\n", SELECTION),
+    ("selection: final block left out", ("selection_rows_ref",),
+     "        for e in range(last):\n            out.append(base + (nb - 1) * block_size + e)\n", "", SELECTION),
+    ("block-granular table puts the final block first", ("selection_pages_ref",),
+     "pages += [r * blocks_per_request + j for j in sel] + [r * blocks_per_request + nb - 1]",
+     "pages += [r * blocks_per_request + nb - 1] + [r * blocks_per_request + j for j in sel]", SELECTION),
+    ("second K stream: the extra score term dropped", ("attention_extra", "partials_extra"),
+     "s = scale * (qr @ K.T + qer @ Ke.T)", "s = scale * (qr @ K.T)", (test_extra_pins,)),
+    ("second K stream: LSE in natural log", ("attention_extra", "partials_extra"),
+     "return (w / tot) @ V, (m[:, 0] + np.log(tot[:, 0])) / np.log(2.0)",
+     "return (w / tot) @ V, m[:, 0] + np.log(tot[:, 0])", (test_extra_pins,)),
+]
+
+
+def _pin_calls(modules=(pins,)):
+    """Every pin of `modules` (a module, or (module, the names of the pins to take)) as (name, function,
+    kwargs), parametrize marks expanded; pins that take fixtures are left out."""
     calls = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
-        if not name.startswith("test_") or fn.__module__ != pins.__name__:
+    for mod in modules:
+        mod, only = mod if isinstance(mod, tuple) else (mod, None)
+        calls += [c for c in _module_pin_calls(mod) if only is None or c[0] in only]
+    return calls
+
+
+def _module_pin_calls(mod):
+    calls = []
+    for name, fn in inspect.getmembers(mod, inspect.isfunction):
+        if not name.startswith("test_") or fn.__module__ != mod.__name__:
             continue
         grids = []
         for mark in getattr(fn, "pytestmark", []):
@@ -100,14 +146,40 @@ def _first_failing_pin(src_text, workdir, tag):
     try:
         oracle.build(force=True)  # outside the pins: a mutant that does not compile is an error, not a catch
         oracle.lib()
-        for name, fn, kw in _pin_calls():
-            try:
-                fn(**kw)
-            except Exception:  # noqa: BLE001 -- any failure (assertion or error) counts as caught
-                return f"{name}{kw or ''}"
-        return None
+        return _run_pins(_pin_calls())
     finally:
         oracle._SRC, oracle._LIB_PATH, oracle._lib = saved
+
+
+def _run_pins(calls):
+    for name, fn, kw in calls:
+        try:
+            fn(**kw)
+        except Exception:  # noqa: BLE001 -- any failure (assertion or error) counts as caught
+            return f"{name}{kw or ''}"
+    return None
+
+
+def _python_mutant_catch(text, names, modules, workdir, tag):
+    """Load `text` as a copy of the oracle package (beside a copy of its C source), swap its functions
+    `names` into the oracle, and return the first pin of `modules` that fails (None if all pass)."""
+    d = os.path.join(workdir, tag)
+    os.makedirs(d, exist_ok=True)
+    shutil.copy(SRC, os.path.join(d, "pa_oracle.c"))
+    path = os.path.join(d, "__init__.py")
+    with open(path, "w") as f:
+        f.write(text)
+    mod = types.ModuleType("oracle_" + tag)
+    mod.__file__ = path
+    exec(compile(text, path, "exec"), mod.__dict__)
+    saved = {n: getattr(oracle, n) for n in names}
+    try:
+        for n in names:
+            setattr(oracle, n, getattr(mod, n))
+        return _run_pins(_pin_calls(modules))
+    finally:
+        for n, f in saved.items():
+            setattr(oracle, n, f)
 
 
 @pytest.fixture(scope="module")
@@ -129,5 +201,23 @@ def test_planted_oracle_mistake_fails_a_pin(workdir, what, old, new):
     assert text.count(old) == 1, f"mutation target not found exactly once: {old!r}"
     tag = "m%08x" % (abs(hash(what)) & 0xFFFFFFFF)
     caught = _first_failing_pin(text.replace(old, new), workdir, tag)
+    assert caught is not None, f"no pin catches: {what}"
+    print(f"{what}: caught by {caught}")
+
+
+def test_unmutated_python_oracle_passes_every_pin_through_the_runner(workdir):
+    text = open(OracleSrc).read()
+    names = sorted({n for m in PY_MUTANTS for n in m[1]})
+    modules = tuple({id(m): m for mut in PY_MUTANTS for m in mut[4]}.values())
+    assert len(_pin_calls(modules)) >= 50
+    assert _python_mutant_catch(text, names, modules, workdir, "pyclean") is None
+
+
+@pytest.mark.parametrize("what,names,old,new,modules", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_python_oracle_mistake_fails_a_pin(workdir, what, names, old, new, modules):
+    text = open(OracleSrc).read()
+    assert text.count(old) == 1, f"mutation target not found exactly once: {old!r}"
+    tag = "p%08x" % (abs(hash(what)) & 0xFFFFFFFF)
+    caught = _python_mutant_catch(text.replace(old, new), names, modules, workdir, tag)
     assert caught is not None, f"no pin catches: {what}"
     print(f"{what}: caught by {caught}")
