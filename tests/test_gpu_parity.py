@@ -160,6 +160,35 @@ def test_cascade_staging_paths_and_head_dims(ps, D, dt):
     assert_close(out, lse, flat_o, flat_l, f"cascade vs flat ps={ps} D={D}")
 
 
+@pytest.mark.parametrize("members,Hq,Hkv,dt", [(2, 16, 4, torch.float16), (4, 32, 8, torch.bfloat16),
+                                               (2, 32, 2, torch.float16), (3, 32, 2, torch.bfloat16)])
+def test_cascade_level_tile_widths(members, Hq, Hkv, dt):
+    """Each level of the one-launch cascade runs with its own n-tile count: 8 stacked heads at level 0 and
+    4 at level 1 (one tile each), 16 and 4 (two and one), 32 and 16 (two tiles each, level 0 in two
+    q-groups), 48 and 16; against the oracle's cascade and flat attention."""
+    from paged_attention_decode_gb300 import cascade as C
+    cb = W.cascade_shared_prefix(members=members, prefix_tokens=16 * 40, suffix_range=(20, 300), num_qo_heads=Hq,
+                                 num_kv_heads=Hkv, head_dim=128, dtype=dt, seed=80 + members + Hkv)
+    f = cb.flat
+    M = f.q.shape[0]
+    fp1 = torch.zeros(M, dtype=torch.int32)
+    cp = C.cascade_plan(len(cb.prefix_indices), cb.suffix_indptr, cb.suffix_last_page_len, fp1, 16, Hq, Hkv, 128,
+                        pa.KV_DTYPES[dt], 152, cb.suffix_lens)
+    dev = "cuda"
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = C.cascade_decode(cp, f.q.to(dev), f.k_pool.to(dev), f.v_pool.to(dev), cb.prefix_indices.to(dev),
+                                cb.suffix_indices.to(dev), cb.suffix_indptr.to(dev), cb.suffix_last_page_len.to(dev),
+                                fp1.to(dev), f.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.cascade_ref(f.q, f.k_pool, f.v_pool, cb.prefix_indices, cb.suffix_indices,
+                                      cb.suffix_indptr, cb.suffix_last_page_len, f.scale)
+    assert_close(out, lse, ref_o, ref_l, f"cascade M={members} G={Hq // Hkv}")
+    flat_o, flat_l = oracle.attention(f.q, f.k_pool, f.v_pool, f.indices, f.indptr, f.last_page_len,
+                                      f.first_page_offset, f.scale)
+    assert_close(out, lse, flat_o, flat_l, f"cascade vs flat M={members} G={Hq // Hkv}")
+
+
 def test_cascade_row_map_past_the_merge_input_is_refused_on_the_device():
     """A part_rows entry pointing past the merge input: the kernel writes nothing there and records
     PA_DEVICE_BAD_INDPTR (the host cannot see device row maps)."""
