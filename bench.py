@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sets", type=int, default=3, help="rotating input sets (L2 avoidance)")
     ap.add_argument("--graph", type=int, default=1, help="replay captured CUDA graphs of the steps")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=5000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip timing the other four workloads")

@@ -80,6 +80,18 @@ __device__ __forceinline__ void partial_tc_body(const CUtensorMap& tm_k, const C
   // it waits for this grid to finish
   pdl_launch_dependents();
 
+  // the warp's stage barriers: shared memory only, so set up while the kernel
+  // before this one may still be running
+  uint64_t* mybar = bars + warp * NSW;
+  if (USE_TMA) {
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < NSW; ++s) mbar_init(&mybar[s], 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+  }
+
   // Before the wait, while the kernel before this one may still be running
   // (its last CTAs, or the merge of the step before): warm L2 with this warp's
   // first stage, from a speculative read of the chunk geometry and of the
@@ -124,18 +136,8 @@ __device__ __forceinline__ void partial_tc_body(const CUtensorMap& tm_k, const C
   unsigned char* mst = smem + warp * NSW * L::STAGE;
   unsigned short* pt_hi = reinterpret_cast<unsigned short*>(smem + L::BODY + warp * 2 * HP * 32);
   unsigned short* pt_lo = pt_hi + HP * 16;
-  uint64_t* mybar = bars + warp * NSW;
   const uint64_t policy = policy_evict_first();
   const int box_rows = ps <= kStageRows ? ps : kStageRows;
-
-  if (USE_TMA) {
-    if (lane == 0) {
-#pragma unroll
-      for (int s = 0; s < NSW; ++s) mbar_init(&mybar[s], 1);
-      fence_barrier_init();
-    }
-    __syncwarp();
-  }
 
   // ---- staging ----
   // Lane (lane & 15) holds the page id of page (lane & 15) of stage j, or -1.
